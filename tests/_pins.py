@@ -1,0 +1,232 @@
+"""Independent checks ("pins") for the CPU oracle.
+
+Each check compares an attention or acceptance function against something that does
+not reuse its code: a library routine (``torch.nn.functional.
+scaled_dot_product_attention`` and ``scipy.special.logsumexp`` on CPU, float64) applied
+to an independently materialised sequence, a closed form, or an exhaustive
+enumeration.  The checks take the function under test as an argument so that
+``test_oracle_mutations.py`` can show each one fails on a planted mistake.
+"""
+from __future__ import annotations
+
+import itertools
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+from scipy.special import logsumexp
+
+
+def all_parent_arrays(m: int):
+    """Every topologically ordered parent array of m nodes: parent[i] in {-1..i-1}."""
+    return itertools.product(*[range(-1, i) for i in range(m)])
+
+
+def random_problem(rng, P, m, Hq=4, Hkv=2, d=8, parent=None):
+    """Float64 inputs of one sequence (B = 1)."""
+    q = rng.standard_normal((m, Hq, d))
+    kc = rng.standard_normal((P, Hkv, d))
+    vc = rng.standard_normal((P, Hkv, d))
+    tk = rng.standard_normal((m, Hkv, d))
+    tv = rng.standard_normal((m, Hkv, d))
+    if parent is None:
+        parent = np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, m)], dtype=np.int32)
+    return dict(q=q, k_cache=kc, v_cache=vc, tree_k=tk, tree_v=tv,
+                parent=np.asarray(parent, dtype=np.int32),
+                cu_prefix=np.array([0, P], dtype=np.int32),
+                cu_nodes=np.array([0, m], dtype=np.int32), num_kv_heads=Hkv)
+
+
+def path_to(parent, i):
+    """Node ids on the path root -> i (inclusive)."""
+    path = []
+    while i >= 0:
+        path.append(i)
+        i = int(parent[i])
+    return path[::-1]
+
+
+def causal_last_row(prob, i):
+    """Causal attention at the last position of the materialised sequence
+    prefix ++ path(root -> i), every query head; returns (o [Hq, d], lse [Hq]).
+
+    The sequence is built explicitly; attention is the library's causal SDPA on it,
+    with KV heads expanded in contiguous groups (head h reads KV head h // G)."""
+    parent = prob["parent"]
+    path = path_to(parent, i)
+    Kseq = np.concatenate([prob["k_cache"], prob["tree_k"][path]], axis=0)   # [L, Hkv, d]
+    Vseq = np.concatenate([prob["v_cache"], prob["tree_v"][path]], axis=0)
+    L, Hkv, d = Kseq.shape
+    Hq = prob["q"].shape[1]
+    G = Hq // Hkv
+    # queries: filler rows for earlier positions, the node's own query last
+    rng = np.random.default_rng(7)
+    Qseq = rng.standard_normal((L, Hq, d))
+    Qseq[-1] = prob["q"][i]
+    qt = torch.from_numpy(Qseq).permute(1, 0, 2)                          # [Hq, L, d]
+    kt = torch.from_numpy(Kseq).permute(1, 0, 2).repeat_interleave(G, dim=0)
+    vt = torch.from_numpy(Vseq).permute(1, 0, 2).repeat_interleave(G, dim=0)
+    o = F.scaled_dot_product_attention(qt, kt, vt, is_causal=True)       # [Hq, L, d]
+    logits = (qt[:, -1:, :] @ kt.transpose(1, 2))[:, 0, :].numpy() / np.sqrt(d)
+    lse = logsumexp(logits, axis=1)
+    return o[:, -1, :].numpy(), lse
+
+
+def check_path_bruteforce(attn_fn, prob, rtol=1e-11, atol=1e-11):
+    """Every node's output/LSE equals causal attention over prefix ++ its path."""
+    out, lse = attn_fn(**prob)
+    for i in range(prob["q"].shape[0]):
+        o_ref, l_ref = causal_last_row(prob, i)
+        np.testing.assert_allclose(out[i], o_ref, rtol=rtol, atol=atol)
+        np.testing.assert_allclose(lse[i], l_ref, rtol=rtol, atol=atol)
+
+
+def check_chain_is_causal(attn_fn, rng, P=13, m=7, Hq=4, Hkv=2, d=8):
+    """A chain tree is ordinary causal attention over prefix ++ chain (one SDPA call)."""
+    prob = random_problem(rng, P, m, Hq, Hkv, d, parent=np.arange(-1, m - 1))
+    out, lse = attn_fn(**prob)
+    G = Hq // Hkv
+    K = np.concatenate([prob["k_cache"], prob["tree_k"]], 0)
+    V = np.concatenate([prob["v_cache"], prob["tree_v"]], 0)
+    Q = np.concatenate([np.zeros((P, Hq, d)), prob["q"]], 0)
+    qt = torch.from_numpy(Q).permute(1, 0, 2)
+    kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(G, 0)
+    vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(G, 0)
+    o = F.scaled_dot_product_attention(qt, kt, vt, is_causal=True)[:, P:, :].permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(out, o, rtol=1e-11, atol=1e-11)
+    logits = (qt @ kt.transpose(1, 2)).numpy() / np.sqrt(d)               # [Hq, L, L]
+    Ltot = P + m
+    causal = np.tril(np.ones((Ltot, Ltot), dtype=bool))
+    lref = logsumexp(np.where(causal[None], logits, -np.inf), axis=2)[:, P:].T
+    np.testing.assert_allclose(lse, lref, rtol=1e-11, atol=1e-11)
+
+
+def check_single_node_is_decode(attn_fn, rng, P=29, Hq=4, Hkv=2, d=8):
+    """m = 1: plain decode attention over prefix ++ the node's own key."""
+    prob = random_problem(rng, P, 1, Hq, Hkv, d, parent=[-1])
+    out, lse = attn_fn(**prob)
+    G = Hq // Hkv
+    K = np.concatenate([prob["k_cache"], prob["tree_k"]], 0)
+    V = np.concatenate([prob["v_cache"], prob["tree_v"]], 0)
+    qt = torch.from_numpy(prob["q"]).permute(1, 0, 2)                    # [Hq, 1, d]
+    kt = torch.from_numpy(K).permute(1, 0, 2).repeat_interleave(G, 0)
+    vt = torch.from_numpy(V).permute(1, 0, 2).repeat_interleave(G, 0)
+    o = F.scaled_dot_product_attention(qt, kt, vt)[:, 0, :].numpy()
+    np.testing.assert_allclose(out[0], o, rtol=1e-11, atol=1e-11)
+
+
+def check_uniform_closed_form(attn_fn, rng, P=9, Hq=2, Hkv=1, d=4):
+    """All keys equal => softmax uniform over the visible keys:
+    out = mean of the visible values and lse = z + log(#visible)."""
+    m = 5
+    parent = np.array([-1, 0, 1, 0, -1], dtype=np.int32)   # depths 1,2,3,2,1
+    prob = random_problem(rng, P, m, Hq, Hkv, d, parent=parent)
+    key = rng.standard_normal(d)
+    prob["k_cache"][:] = key
+    prob["tree_k"][:] = key
+    out, lse = attn_fn(**prob)
+    for i in range(m):
+        path = path_to(parent, i)
+        vis_v = np.concatenate([prob["v_cache"][:, 0], prob["tree_v"][path, 0]], 0)
+        for h in range(Hq):
+            z = prob["q"][i, h] @ key / np.sqrt(d)
+            np.testing.assert_allclose(out[i, h], vis_v.mean(0), rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(lse[i, h], z + np.log(P + len(path)), rtol=1e-12, atol=1e-12)
+
+
+def check_sibling_independence(attn_fn, rng, P=5):
+    """Changing node j's key/value moves exactly the nodes that have j on their path."""
+    parent = np.array([-1, 0, 0, 1, 2, -1, 5], dtype=np.int32)
+    prob = random_problem(rng, P, len(parent), parent=parent)
+    out0, lse0 = attn_fn(**prob)
+    for j in range(len(parent)):
+        p2 = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in prob.items()}
+        p2["tree_k"][j] += 1.0
+        p2["tree_v"][j] -= 1.0
+        out1, lse1 = attn_fn(**p2)
+        for i in range(len(parent)):
+            sees = j in path_to(parent, i)
+            same = np.array_equal(out0[i], out1[i]) and np.array_equal(lse0[i], lse1[i])
+            assert same != sees, (i, j, sees)
+
+
+def check_relabeling(attn_fn, rng, P=6):
+    """Two topological orders of one tree give the same per-node results."""
+    parent = np.array([-1, 0, 0, 1, 1, 2, -1], dtype=np.int32)
+    prob = random_problem(rng, P, len(parent), parent=parent)
+    out, lse = attn_fn(**prob)
+    perm = np.array([6, 0, 2, 5, 1, 4, 3])           # new position -> old id, parents first
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    new_parent = np.array([-1 if parent[o] < 0 else inv[parent[o]] for o in perm], dtype=np.int32)
+    assert all(new_parent[i] < i for i in range(len(perm)))
+    p2 = dict(prob)
+    for k in ("q", "tree_k", "tree_v"):
+        p2[k] = prob[k][perm]
+    p2["parent"] = new_parent
+    out2, lse2 = attn_fn(**p2)
+    np.testing.assert_allclose(out2, out[perm], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse[perm], rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------------ acceptance pins
+
+def forward_greedy_path_check(parent, draft, slot, i):
+    """Is the root -> i path accepted?  Walk it forwards the way a decoder would: the
+    target's greedy token at the prefix end is slot[0]; after accepting node u the next
+    greedy token is slot[u + 1]."""
+    expect = slot[0]
+    for u in path_to(parent, i):
+        if draft[u] != expect:
+            return False
+        expect = slot[u + 1]
+    return True
+
+
+def bruteforce_accept(parent, draft, slot):
+    """Longest accepted path by enumerating every root -> node path; ties -> smaller id."""
+    m = len(parent)
+    best = None
+    for i in range(m):
+        if forward_greedy_path_check(parent, draft, slot, i):
+            path = path_to(parent, i)
+            if best is None or len(path) > len(best[1]):
+                best = (i, path)
+    if best is None:
+        return 0, [], int(slot[0])
+    return len(best[1]), best[1], int(slot[best[0] + 1])
+
+
+def check_accept_bruteforce(accept_fn, rng, max_m=6, vocab=2, draws=2):
+    for m in range(1, max_m + 1):
+        for parent in all_parent_arrays(m):
+            parent = np.asarray(parent, dtype=np.int32)
+            for _ in range(draws):
+                slot = rng.integers(0, vocab, m + 1).astype(np.int32)
+                draft = rng.integers(0, vocab, m).astype(np.int32)
+                alen, apath, nxt = accept_fn(parent, draft, slot, np.array([0, m], np.int32))
+                L, path, tok = bruteforce_accept(parent, draft, slot)
+                assert int(alen[0]) == L, (parent, draft, slot)
+                assert list(apath[:L]) == path
+                assert all(apath[L:] == -1)
+                assert int(nxt[0]) == tok
+
+
+def chain_expected_tokens_by_enumeration(accept_fn, conditional):
+    """Sum over all 2^gamma match patterns of Pr(pattern) * (accept_len + 1) on a chain.
+
+    Position k matches independently with probability conditional[k]; only the
+    matched prefix matters to the walk, so Pr(accept_len >= k) is the running product
+    of the conditional probabilities, i.e. the page's survival value s_k."""
+    gamma = len(conditional)
+    parent = np.arange(-1, gamma - 1, dtype=np.int32)
+    slot = np.arange(100, 100 + gamma + 1, dtype=np.int32)
+    total = 0.0
+    for bits in itertools.product([0, 1], repeat=gamma):
+        pr = 1.0
+        for c, b in zip(conditional, bits):
+            pr *= c if b else (1.0 - c)
+        draft = np.array([slot[parent[k] + 1] if bits[k] else -5 for k in range(gamma)], np.int32)
+        alen, _, _ = accept_fn(parent, draft, slot, np.array([0, gamma], np.int32))
+        total += pr * (int(alen[0]) + 1)
+    return total

@@ -1,0 +1,149 @@
+"""Each pin must catch a plausible mistake planted in the oracle (on the CPU).
+
+The mutants below are the real oracle with one thing changed: the node's own key
+masked out, a proper-ancestor slip, the wrong softmax scale, the wrong GQA mapping, the
+tree K/V swapped, the prefix dropped, an LSE term dropped, ties broken the other way,
+the bonus token read from the wrong slot.  Every one must make at least one pin fail."""
+import numpy as np
+import pytest
+
+import oracle.tree_attention as ta
+from oracle import accept_longest_path, attention_partial, merge_partials, tree_verify_attention
+from tests import _pins
+
+
+def _attention_pins_fail(fn):
+    rng = np.random.default_rng(0)
+    checks = [
+        lambda: [_pins.check_path_bruteforce(fn, _pins.random_problem(rng, P, m, parent=par))
+                 for P in (0, 5) for m in range(1, 5) for par in _pins.all_parent_arrays(m)],
+        lambda: _pins.check_chain_is_causal(fn, rng),
+        lambda: _pins.check_single_node_is_decode(fn, rng),
+        lambda: _pins.check_uniform_closed_form(fn, rng),
+        lambda: _pins.check_sibling_independence(fn, rng),
+    ]
+    failed = 0
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            failed += 1
+    return failed
+
+
+def test_real_oracle_passes_all_attention_pins():
+    assert _attention_pins_fail(tree_verify_attention) == 0
+
+
+def test_mutant_self_not_visible(monkeypatch):
+    real = ta.ancestor_mask
+
+    def no_self(parent):
+        v = real(parent)
+        np.fill_diagonal(v, False)
+        return v
+    monkeypatch.setattr(ta, "ancestor_mask", no_self)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        assert _attention_pins_fail(ta.tree_verify_attention) > 0
+
+
+def test_mutant_parent_only_instead_of_all_ancestors(monkeypatch):
+    def parent_and_self(parent):
+        m = len(parent)
+        v = np.eye(m, dtype=bool)
+        for i, p in enumerate(parent):
+            if p >= 0:
+                v[i, p] = True
+        return v
+    monkeypatch.setattr(ta, "ancestor_mask", parent_and_self)
+    assert _attention_pins_fail(ta.tree_verify_attention) > 0
+
+
+def test_mutant_wrong_scale():
+    fn = lambda **p: tree_verify_attention(**p, softmax_scale=1.0 / 8)  # 1/d instead of 1/sqrt(d)  # noqa: E731
+    assert _attention_pins_fail(fn) > 0
+
+
+def test_mutant_wrong_gqa_mapping():
+    def fn(**p):
+        Hq = p["q"].shape[1]
+        Hkv = p["num_kv_heads"]
+        G = Hq // Hkv
+        # interleaved mapping h -> h % Hkv, emulated by permuting the query heads
+        perm = np.array([(h % Hkv) * G + h // Hkv for h in range(Hq)])
+        inv = np.argsort(perm)
+        q2 = p["q"][:, inv, :]
+        out, lse = tree_verify_attention(**{**p, "q": q2})
+        return out[:, perm, :], lse[:, perm]
+    assert _attention_pins_fail(fn) > 0
+
+
+def test_mutant_tree_k_v_swapped():
+    fn = lambda **p: tree_verify_attention(**{**p, "tree_k": p["tree_v"], "tree_v": p["tree_k"]})  # noqa: E731
+    assert _attention_pins_fail(fn) > 0
+
+
+def test_mutant_prefix_dropped():
+    def fn(**p):
+        z = p["k_cache"][:0]
+        out, lse = tree_verify_attention(**{**p, "k_cache": z, "v_cache": z,
+                                           "cu_prefix": np.zeros_like(p["cu_prefix"])})
+        return out, lse
+    assert _attention_pins_fail(fn) > 0
+
+
+def test_mutant_merge_without_reweighting():
+    rng = np.random.default_rng(1)
+    q, K, V = rng.standard_normal(8), rng.standard_normal((30, 8)), rng.standard_normal((30, 8))
+    parts = [attention_partial(q, K[a:b], V[a:b], 0.35) for a, b in [(0, 11), (11, 30)]]
+    o_ref, l_ref = attention_partial(q, K, V, 0.35)
+    o, lse = merge_partials(np.stack([p[0] for p in parts]), np.array([p[1] for p in parts]))
+    assert np.allclose(o, o_ref, rtol=1e-12)
+    bad = sum(p[0] for p in parts) / 2   # plain average: the planted mistake
+    assert not np.allclose(bad, o_ref, rtol=1e-6)
+
+
+def _accept_pins_fail(fn):
+    failed = 0
+    try:
+        _pins.check_accept_bruteforce(fn, np.random.default_rng(0), max_m=5, vocab=2, draws=2)
+    except AssertionError:
+        failed += 1
+    ey = _pins.chain_expected_tokens_by_enumeration(fn, [0.85, 0.75, 0.60, 0.40])
+    if abs(ey - 3.023) > 1e-12:
+        failed += 1
+    return failed
+
+
+def test_real_acceptance_passes_pins():
+    assert _accept_pins_fail(accept_longest_path) == 0
+
+
+def _walk_variant(parent, draft, slot, cu, tie_later=False, own_slot=False, bonus_shift=1):
+    """A copy of the oracle's walk (one sequence) with switchable planted mistakes."""
+    m = len(parent)
+    best, bd = -1, 0
+    for i in range(m):
+        j, ok, depth = i, True, 0
+        while j >= 0:
+            want = slot[j] if own_slot else slot[parent[j] + 1]
+            ok &= bool(draft[j] == want)
+            depth += 1
+            j = int(parent[j])
+        if ok and (depth > bd or (tie_later and depth == bd)):
+            best, bd = i, depth
+    path = np.full(m, -1, np.int32)
+    if best >= 0:
+        pth = _pins.path_to(parent, best)
+        path[: len(pth)] = pth
+    nxt = slot[best + bonus_shift] if best >= 0 else slot[0]
+    return np.array([bd], np.int32), path, np.array([nxt], np.int32)
+
+
+def test_walk_copy_without_mistakes_passes():
+    assert _accept_pins_fail(_walk_variant) == 0
+
+
+@pytest.mark.parametrize("mistake", [dict(tie_later=True), dict(own_slot=True), dict(bonus_shift=0)])
+def test_acceptance_mutants_are_caught(mistake):
+    assert _accept_pins_fail(lambda *a: _walk_variant(*a, **mistake)) > 0
