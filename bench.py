@@ -1,0 +1,427 @@
+"""Throughput of the tree-verification hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic inputs:
+attention partials (prefix split-KV + masked tree tile), the log-sum-exp combine, and
+the greedy acceptance walk.  Default workload: B=1, Hq=32, Hkv=8, d=128, bf16,
+prefix 65536, 64-node best-first tree (width 4, depth <= 8).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is tree nodes verified per second over all
+ranks (each rank runs its own copy of the workload: weak scaling).  The L2 cache is
+flushed (256 MiB write) before every timed step, outside the timed interval.
+`--impl reference` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify attn nodes/s & prefix-KV GB/s (1×GB300), fraction of roofline"
+
+
+def algorithmic_bytes(w):
+    """Bytes the method must move (bf16 storage): prefix K+V, tree K+V, Q, parent
+    (read by the partials kernel) and out + lse (written by the combine)."""
+    es = 2 if w.dtype == "bf16" else 4
+    d, Hq, Hkv, N = w.head_dim, w.num_q_heads, w.num_kv_heads, w.num_nodes
+    prefix_kv = int(w.cu_prefix[-1]) * Hkv * d * es * 2
+    k1 = prefix_kv + N * Hkv * d * es * 2 + N * Hq * d * es + 4 * N
+    total = k1 + N * Hq * d * es + N * Hq * 4
+    return prefix_kv, k1, total
+
+
+def algorithmic_flops(w):
+    d, Hq = w.head_dim, w.num_q_heads
+    from tree_verification_attention_gb300.workloads import tree_depths
+    f = 0
+    for b in range(w.batch):
+        n0, n1 = int(w.cu_nodes[b]), int(w.cu_nodes[b + 1])
+        P = int(w.cu_prefix[b + 1] - w.cu_prefix[b])
+        depths = tree_depths(w.parent[n0:n1])
+        f += 4 * d * Hq * ((n1 - n0) * P + int(depths.sum()))
+    return f
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tree_verification_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per launch of the partials kernel from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload_name and parts[2] == src:
+                return int(parts[1])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus and world > 1:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    return rank, world, local
+
+
+def cpu_oracle_sample(w, kv_heads, repeats):
+    """Oracle on the rows of the first `kv_heads` KV heads (all nodes), `repeats` times;
+    returns (seconds per repeat, node-equivalents per repeat)."""
+    import oracle
+    G = w.num_q_heads // w.num_kv_heads
+    k = kv_heads
+    q = w.f64("q")[:, : G * k]
+    kc = w.f64("k_cache")[:, :k]
+    vc = w.f64("v_cache")[:, :k]
+    tk = w.f64("tree_k")[:, :k]
+    tv = w.f64("tree_v")[:, :k]
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.tree_verify_attention(q, kc, vc, w.cu_prefix, tk, tv, w.parent, w.cu_nodes, k, w.softmax_scale)
+        oracle.accept_longest_path(w.parent, w.draft_tok, w.target_argmax, w.cu_nodes)
+    dt = (time.perf_counter() - t0) / repeats
+    return dt, w.num_nodes * k / w.num_kv_heads
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    # bounded sample: one KV head's rows (all nodes) per step; the node count is scaled by
+    # the fraction of query heads covered so the unit stays nodes/s of the full problem
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, 1, 1)
+    times = []
+    for _ in range(args.steps):
+        dt, nodes = cpu_oracle_sample(w, 1, 1)
+        times.append(dt)
+    sec = float(np.mean(times))
+    value = nodes / sec
+    sample = (f"oracle (float64 numpy) on all {w.num_nodes} nodes x the {w.num_q_heads // w.num_kv_heads} "
+              f"query heads of 1 of {w.num_kv_heads} KV heads per step, + acceptance walk")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "prefix_len": [int(x) for x in w.prefix_lens][:8], "tree_nodes": int(w.tree_sizes.max())},
+        "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="rough budget of host-core seconds for the cpu_baseline sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank, world, local = dist_setup(args.gpus)
+    from tree_verification_attention_gb300 import workloads
+    w = workloads.make_workload(args.config)
+
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            if rank == 0:
+                run_reference(args, w, rank)
+            dist.barrier()
+            dist.destroy_process_group()
+        else:
+            run_reference(args, w, rank)
+        return
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from tree_verification_attention_gb300 import api
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    # ---- device-resident inputs
+    def f(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if w.dtype == "bf16":
+            t = t.view(torch.int16).view(torch.bfloat16)
+        return t
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32))
+
+    host = dict(q=f(w.q), k_cache=f(w.k_cache), v_cache=f(w.v_cache), tree_k=f(w.tree_k),
+                tree_v=f(w.tree_v), parent=i32(w.parent), cu_prefix=i32(w.cu_prefix),
+                cu_nodes=i32(w.cu_nodes), draft_tok=i32(w.draft_tok), target_argmax=i32(w.target_argmax))
+    d = {k: v.to(dev) for k, v in host.items()}
+    max_prefix = int(w.prefix_lens.max())
+    max_nodes = int(w.tree_sizes.max())
+    params = api.make_params(d["q"], d["k_cache"], d["cu_prefix"], d["cu_nodes"], w.num_kv_heads,
+                             max_prefix, max_nodes)
+    ws = api.alloc_workspace(params, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+    B, N = w.batch, w.num_nodes
+    alen = torch.empty(B, dtype=torch.int32, device=dev)
+    apath = torch.empty(N, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(src):
+        api.tree_verify_attn_partials(src["q"], src["k_cache"], src["v_cache"], src["tree_k"], src["tree_v"],
+                                      src["parent"], src["cu_prefix"], src["cu_nodes"], max_prefix, max_nodes,
+                                      ws, status, params=params)
+
+    def rest(src):
+        api.tree_verify_attn_combine(params, ws, out, lse, status)
+        api.accept_longest_path(src["cu_nodes"], src["parent"], src["draft_tok"], src["target_argmax"],
+                                alen, apath, nxt, status)
+
+    for _ in range(args.warmup):
+        step(d)
+        rest(d)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())} during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid) if hasattr(
+        torch.cuda.get_device_properties(dev), "uuid") else str(local)
+    sampler = ClockSampler(gpu_id)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda._sleep(int(20e6))  # host enqueues ahead of the GPU: no launch gaps in the timings
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step(d)
+        ev[i][1].record(stream)
+        rest(d)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    k1_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ms = float(np.mean(step_ms))
+    k1 = float(np.mean(k1_ms))
+    if world > 1:
+        t = torch.tensor([ms, k1], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, k1 = float(t[0]), float(t[1])
+
+    # ---- end to end through the public API from pinned host buffers
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    h_acc = [torch.empty(B, dtype=torch.int32).pin_memory(), torch.empty(N, dtype=torch.int32).pin_memory(),
+             torch.empty(B, dtype=torch.int32).pin_memory()]
+    d2 = {k: torch.empty_like(v) for k, v in d.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * 4 + (2 * B + N) * 4
+
+    def e2e_step():
+        for k in d2:
+            d2[k].copy_(pinned[k], non_blocking=True)
+        step(d2)
+        rest(d2)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+        h_acc[0].copy_(alen, non_blocking=True)
+        h_acc[1].copy_(apath, non_blocking=True)
+        h_acc[2].copy_(nxt, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = max(3, K // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda._sleep(int(20e6))
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    if int(status.item()) != 0:
+        raise SystemExit(f"device status {int(status.item())}")
+
+    # ---- CPU oracle baseline (rank 0 only), bounded sample
+    cpu = None
+    if rank == 0:
+        dt1, nodes1 = cpu_oracle_sample(w, 1, 1)
+        reps = max(1, min(20, int(args.cpu_seconds / max(dt1, 1e-3))))
+        dt, nodes = cpu_oracle_sample(w, 1, reps)
+        cpu = {"value": nodes / dt, "unit": "nodes/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{reps}x: all {w.num_nodes} nodes x the {w.num_q_heads // w.num_kv_heads} query heads "
+                         f"of 1 of {w.num_kv_heads} KV heads (node count scaled by 1/{w.num_kv_heads}), "
+                         f"float64 numpy, + acceptance walk"}
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    hbm_peak, tc_peak, peak_kind = load_peaks()
+    prefix_kv, k1_bytes, total_bytes = algorithmic_bytes(w)
+    flops = algorithmic_flops(w)
+    k1_gbs = k1_bytes / (k1 * 1e-3) / 1e9
+    roof_s = max(total_bytes / (hbm_peak * 1e9), flops / (tc_peak * 1e12))
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC,
+        "value": world * N / (ms * 1e-3),
+        "unit": "nodes/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": B, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "prefix_len": [int(x) for x in w.prefix_lens][:8], "tree_nodes": int(w.tree_sizes.max()),
+                   "seed": w.seed, "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every timed step (256 MiB write, untimed)"},
+        "prefix_kv_gbs": prefix_kv / (ms * 1e-3) / 1e9,
+        "step_roofline_frac": roof_s / (ms * 1e-3),
+        "roofline": {"bound": "hbm", "kernel": "partials (prefix split-KV + tree tile)",
+                     "achieved": k1_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": k1_gbs / hbm_peak,
+                     "traffic": traffic, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes": k1_bytes, "us_per_launch": k1 * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,177 @@
+/*
+ * tva.h - tree-verification attention and greedy tree acceptance (C ABI).
+ *
+ * The operation (LongSpec, "Fast Tree Attention" section, Hybrid Tree Attention):
+ * every query of a speculative draft tree attends (1) without a mask to the cached
+ * prefix pairs {K_cache, V_cache} and (2) to the tree's own pairs {K_specs, V_specs}
+ * under the tree mask, which lets a node see only its ancestors ("Faster decoding",
+ * section "Chains and trees consume work differently").  The partial results are
+ * combined exactly through their log-sum-exp (same LongSpec section, "Aggregation",
+ * and its appendix "Correctness of attention aggregation").  The greedy verification
+ * contract ("Faster decoding", section on modified rejection sampling, paragraph on
+ * greedy verification) keeps the longest draft path that agrees with the target's
+ * greedy tokens and emits the target's token after it.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers are DEVICE pointers unless a comment says otherwise.  The caller owns
+ *   every buffer; the library never allocates on these paths, except the one
+ *   convenience form that says so (tree_verify_attn), whose workspace tva_release()
+ *   frees.
+ * - All tensors are dense, row-major and contiguous; floating-point base pointers
+ *   must be 16-byte aligned.  Shapes use: B batch, Hq query heads, Hkv KV heads
+ *   (Hq % Hkv == 0, query head h reads KV head h / (Hq / Hkv)), d head_dim,
+ *   P_b prefix length of sequence b, m_b tree size of sequence b, N = sum of m_b.
+ * - Trees: parent[] holds LOCAL node ids; parent[i] == -1 makes node i a child of
+ *   the prefix end; otherwise 0 <= parent[i] < i (topological order).  A node sees
+ *   its ancestors and itself.
+ * - Work is enqueued asynchronously on `stream` (a cudaStream_t; 0 = legacy default
+ *   stream).  Nothing synchronises.
+ * - Errors: argument errors found on the host return a non-zero tva_status and
+ *   enqueue nothing.  Errors only visible on the device (a parent id out of range, a
+ *   cu_* entry beyond the stated bounds, an internal wait that timed out) are
+ *   written to *dev_status (an int32 the caller zeroes; the first error code wins)
+ *   and the affected outputs are left unspecified.  Kernels never trap.
+ */
+#ifndef TVA_H_
+#define TVA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TVA_OK = 0,
+  TVA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, bound exceeded */
+  TVA_ERR_UNSUPPORTED = 2, /* head_dim or dtype this build does not implement      */
+  TVA_ERR_BAD_TREE = 3,    /* parent[i] not in [-1, i)                              */
+  TVA_ERR_WORKSPACE = 4,   /* workspace missing or smaller than tva_workspace_size  */
+  TVA_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute, ...)   */
+  TVA_ERR_TIMEOUT = 6      /* an internal bounded wait expired (device status only) */
+} tva_status;
+
+typedef enum {
+  TVA_BF16 = 0, /* bfloat16 inputs and output, fp32 accumulation */
+  TVA_FP32 = 1  /* float32 inputs and output, fp32 accumulation  */
+} tva_dtype;
+
+/* Problem description for the batched (varlen) entry points. */
+typedef struct {
+  int batch;          /* B >= 1                                                      */
+  int num_q_heads;    /* Hq >= 1                                                     */
+  int num_kv_heads;   /* Hkv >= 1, Hq % Hkv == 0                                     */
+  int head_dim;       /* d: 64 or 128                                                */
+  tva_dtype dtype;    /* q, k_cache, v_cache, tree_k, tree_v and out share it        */
+  float softmax_scale;/* logit scale; 0 selects 1/sqrt(head_dim)                     */
+  const int32_t* cu_prefix; /* device [B+1], cu_prefix[0] = 0, non-decreasing:
+                               sequence b owns k_cache rows cu_prefix[b] ..
+                               cu_prefix[b+1]-1                                       */
+  const int32_t* cu_nodes;  /* device [B+1], cu_nodes[0] = 0, non-decreasing:
+                               sequence b owns nodes (q/tree_k/tree_v/out rows and
+                               parent entries) cu_nodes[b] .. cu_nodes[b+1]-1        */
+  int max_prefix_len; /* host bound: every P_b <= max_prefix_len                     */
+  int max_nodes;      /* host bound: every m_b <= max_nodes <= 128                   */
+  int kv_capacity;    /* rows allocated in k_cache and v_cache (>= cu_prefix[B])     */
+  int node_capacity;  /* rows allocated in q, tree_k, tree_v, out, lse, parent
+                         (>= cu_nodes[B])                                            */
+} tva_params;
+
+/* Bytes of device workspace tree_verify_attn_varlen / _partials / _combine need for
+ * `p` on the current device (it depends on the SM count).  Returns 0 when `p` is
+ * invalid.  The workspace holds float32 partial outputs and log-sum-exps; it needs
+ * no initialisation and its contents between the two stages are private. */
+size_t tva_workspace_size(const tva_params* p);
+
+/* Tree-verification attention over a ragged batch (LongSpec, "Fast Tree Attention").
+ *   q        [N, Hq, d]    queries of the tree nodes (already projected/rotated)
+ *   k_cache, v_cache [kv_capacity, Hkv, d]  cached prefix keys/values, ragged by
+ *            cu_prefix (no mask applies to them)
+ *   tree_k, tree_v   [N, Hkv, d]  keys/values of the tree nodes themselves
+ *   parent   [N] int32     local parent ids per sequence (see conventions)
+ *   out      [N, Hq, d]    attention output, same dtype as q
+ *   lse      [N, Hq] float32  natural log of the sum of exp(scaled logits) over every
+ *            key the row sees (prefix + ancestors + self)
+ *   workspace, workspace_bytes  >= tva_workspace_size(p) bytes, 256-byte aligned
+ *   dev_status  device int32, see conventions
+ * Equivalent to tree_verify_attn_partials followed by tree_verify_attn_combine. */
+tva_status tree_verify_attn_varlen(const tva_params* p, const void* q, const void* k_cache,
+                                   const void* v_cache, const void* tree_k,
+                                   const void* tree_v, const int32_t* parent, void* out,
+                                   float* lse, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, void* stream);
+
+/* Stage 1: attention partials.  Splits the prefix keys of every (sequence, KV head,
+ * row group) into contiguous key ranges spread evenly over the GPU's SMs, adds the
+ * tree keys (under the ancestor mask) as one more range, and writes each range's
+ * output and log-sum-exp (the O_cache / O_specs, LSE_cache / LSE_specs of the
+ * LongSpec aggregation) into `workspace`.  Arguments as for tree_verify_attn_varlen. */
+tva_status tree_verify_attn_partials(const tva_params* p, const void* q, const void* k_cache,
+                                     const void* v_cache, const void* tree_k,
+                                     const void* tree_v, const int32_t* parent,
+                                     void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, void* stream);
+
+/* Stage 2: merges every row's partials with the log-sum-exp rule
+ * LSE = log sum_s exp(LSE_s), out = sum_s O_s * exp(LSE_s - LSE)
+ * (LongSpec, "Aggregation" and appendix Proposition) and writes out / lse.
+ * `workspace` must hold the partials written by stage 1 for the same `p`. */
+tva_status tree_verify_attn_combine(const tva_params* p, const void* workspace,
+                                    size_t workspace_bytes, void* out, float* lse,
+                                    int32_t* dev_status, void* stream);
+
+/* Single-sequence convenience form (B = 1).  prefix_len and num_nodes are host
+ * values; every other pointer is a device pointer laid out as above with B = 1.
+ * The workspace and the cu_* arrays are library-owned: allocated on first use per
+ * device (and grown when a larger problem arrives), released by tva_release().
+ * Because it may allocate, do not call it for the first time inside stream capture.
+ * Device-side errors go to a library-owned status word read by
+ * tva_read_device_status(). */
+tva_status tree_verify_attn(const void* q, const void* k_cache, const void* v_cache,
+                            int prefix_len, const void* tree_k, const void* tree_v,
+                            const int32_t* parent, int num_nodes, int num_q_heads,
+                            int num_kv_heads, int head_dim, tva_dtype dtype, void* out,
+                            float* lse, void* stream);
+
+/* Copies the convenience form's device status into *host_status (a HOST pointer),
+ * synchronising `stream`, and clears it.  TVA_OK when nothing was recorded. */
+tva_status tva_read_device_status(int32_t* host_status, void* stream);
+
+/* Frees the convenience form's library-owned buffers on every device. */
+void tva_release(void);
+
+/* Greedy longest accepted path per sequence ("Faster decoding", greedy contract).
+ *   cu_nodes      [B+1] device, as in tva_params
+ *   parent        [N] int32 local parent ids; draft_tok [N] int32 draft tokens
+ *   target_argmax [N+B] int32: sequence b owns slots cu_nodes[b]+b ..
+ *                 cu_nodes[b+1]+b; its slot 0 is the target's greedy token at the
+ *                 prefix end and slot i+1 the target's greedy token after node i
+ *   accept_len    [B] int32: nodes on the accepted path
+ *   accept_path   [N] int32: per sequence, the accepted local ids root first, then -1
+ *   next_token    [B] int32: slot[last+1] (slot[0] when nothing is accepted), the
+ *                 correction or bonus token, so a cycle emits accept_len+1 tokens
+ * Node i is accepted when it and every ancestor match (draft_tok[j] ==
+ * slot[parent[j]+1]); the deepest accepted node wins and equal depths go to the
+ * smaller local id.  Requires every m_b <= 128 and cu_nodes within node_capacity
+ * (else TVA_ERR_INVALID_ARG in *dev_status for that sequence, whose accept_len and
+ * next_token are then 0 and -1 and whose accept_path is left untouched). */
+tva_status accept_longest_path(int batch, int node_capacity, const int32_t* cu_nodes,
+                               const int32_t* parent,
+                               const int32_t* draft_tok, const int32_t* target_argmax,
+                               int32_t* accept_len, int32_t* accept_path,
+                               int32_t* next_token, int32_t* dev_status, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* tva_status_string(tva_status s);
+
+/* Number of workers (CTAs) the partials stage launches for `p` on the current
+ * device, or -1 when `p` is invalid.  Informational. */
+int tva_num_workers(const tva_params* p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TVA_H_ */

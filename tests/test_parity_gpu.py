@@ -1,0 +1,141 @@
+"""GPU parity: the CUDA path against the float64 oracle, element by element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tree_verification_attention_gb300 import api, workloads
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+# Scaled-down versions of the five workloads: several 128-key tiles plus a ragged tail.
+SMALL = [
+    (1, {}),
+    (1, dict(prefix=1000, m=8)),
+    (2, dict(prefix=1100)),
+    (3, dict(prefix=1500)),
+    (4, dict(prefix=(200, 1300))),
+    (5, dict(prefix=900)),
+]
+
+
+@pytest.mark.parametrize("cfg,over", SMALL, ids=[f"c{c}-{i}" for i, (c, _) in enumerate(SMALL)])
+def test_small_workloads_match_oracle(cfg, over):
+    w = workloads.make_workload(cfg, **over)
+    out, lse, st = _gpu.run_attention(w)
+    assert st == 0
+    o_ref, l_ref = _gpu.oracle_attention(w)
+    _gpu.assert_close(w, out, lse, o_ref, l_ref, f"config {cfg} {over}")
+
+
+EDGE = [
+    dict(batch=1, Hq=4, Hkv=1, d=64, prefix=0, m=1, tree="random", dtype="bf16", vocab=8),
+    dict(batch=1, Hq=4, Hkv=1, d=128, prefix=1, m=3, tree="random", dtype="bf16", vocab=8),
+    dict(batch=1, Hq=8, Hkv=8, d=128, prefix=128, m=128, tree="random", dtype="bf16", vocab=8),
+    dict(batch=1, Hq=64, Hkv=8, d=128, prefix=257, m=128, tree="depth_limited", max_depth=10, dtype="bf16", vocab=8),
+    dict(batch=3, Hq=16, Hkv=2, d=64, prefix=(0, 300), m=17, tree="random", dtype="bf16", vocab=8),
+    dict(batch=2, Hq=6, Hkv=3, d=128, prefix=129, m=40, tree="chain", dtype="fp32", vocab=8),
+    dict(batch=2, Hq=2, Hkv=1, d=64, prefix=(0, 0), m=5, tree="random", dtype="fp32", vocab=8),
+    dict(batch=5, Hq=32, Hkv=8, d=128, prefix=(1, 600), m=1, tree="chain", dtype="bf16", vocab=8),
+]
+
+
+@pytest.mark.parametrize("spec", EDGE, ids=[f"edge{i}" for i in range(len(EDGE))])
+def test_edge_cases_match_oracle(spec):
+    w = workloads.make_workload(1, seed=77, **spec)
+    out, lse, st = _gpu.run_attention(w)
+    assert st == 0
+    o_ref, l_ref = _gpu.oracle_attention(w)
+    _gpu.assert_close(w, out, lse, o_ref, l_ref, str(spec))
+
+
+def test_loose_bounds_and_capacity_do_not_change_results():
+    """max_prefix_len / max_nodes larger than needed, k_cache with spare rows."""
+    w = workloads.make_workload(4, prefix=(50, 400), batch=3, m=20)
+    t = _gpu.to_device(w)
+    out1, lse1, st1 = _gpu.run_attention(w, t)
+    extra = torch.zeros((37,) + tuple(t["k_cache"].shape[1:]), dtype=t["k_cache"].dtype, device="cuda:0")
+    t2 = dict(t, k_cache=torch.cat([t["k_cache"], extra]), v_cache=torch.cat([t["v_cache"], extra]))
+    out2, lse2, st2 = _gpu.run_attention(w, t2, max_prefix=4096, max_nodes=128)
+    assert st1 == 0 and st2 == 0
+    o_ref, l_ref = _gpu.oracle_attention(w)
+    _gpu.assert_close(w, out2, lse2, o_ref, l_ref)
+
+
+def test_bad_tree_sets_device_status():
+    w = workloads.make_workload(3, prefix=300, m=16)
+    t = _gpu.to_device(w)
+    t["parent"][5] = 9   # not an earlier node
+    _, _, st = _gpu.run_attention(w, t)
+    assert st == 3
+
+
+def test_cu_bounds_violation_sets_device_status():
+    w = workloads.make_workload(4, prefix=(100, 300), batch=2, m=8)
+    t = _gpu.to_device(w)
+    _, _, st = _gpu.run_attention(w, t, max_prefix=50)   # every P_b exceeds the bound
+    assert st == 1
+
+
+def test_host_errors_enqueue_nothing():
+    w = workloads.make_workload(1)
+    t = _gpu.to_device(w)
+    p = api.make_params(t["q"], t["k_cache"], t["cu_prefix"], t["cu_nodes"], 1, 256, 8)
+    ws = api.alloc_workspace(p, "cuda:0")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    with pytest.raises(api.TvaError) as e:
+        api.tree_verify_attn_partials(t["q"], t["k_cache"], t["v_cache"], t["tree_k"], t["tree_v"],
+                                      t["parent"], t["cu_prefix"], t["cu_nodes"], 256, 8, ws[:16], st)
+    assert e.value.code == 4
+    p.head_dim = 96
+    assert api.workspace_size(p) == 0
+
+
+def test_single_sequence_convenience_form():
+    w = workloads.make_workload(3, prefix=640, m=33)
+    t = _gpu.to_device(w)
+    out, lse = api.tree_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["tree_k"], t["tree_v"], t["parent"])
+    torch.cuda.synchronize()
+    assert api.read_device_status() == 0
+    o_ref, l_ref = _gpu.oracle_attention(w)
+    _gpu.assert_close(w, out.double().cpu().numpy(), lse.double().cpu().numpy(), o_ref, l_ref)
+    t["parent"][3] = 3
+    api.tree_verify_attn(t["q"], t["k_cache"], t["v_cache"], t["tree_k"], t["tree_v"], t["parent"])
+    assert api.read_device_status() == 3
+    assert api.read_device_status() == 0
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_full_size_sampled_rows(cfg):
+    """Full-size workloads in the bench's launch configuration; the oracle evaluates
+    a sample of rows one at a time."""
+    w = workloads.make_workload(cfg)
+    out, lse, st = _gpu.run_attention(w)
+    assert st == 0
+    rows = _gpu.sample_rows(w, 12, seed=cfg)
+    lazy = (lambda name: _LazyBf16(getattr(w, name))) if w.dtype == "bf16" else w.f64
+    o_ref, l_ref = oracle.tree_verify_attention_rows(
+        rows, w.f64("q"), lazy("k_cache"), lazy("v_cache"), w.cu_prefix, lazy("tree_k"),
+        lazy("tree_v"), w.parent, w.cu_nodes, w.num_kv_heads, w.softmax_scale)
+    sel_o = np.stack([out[n, h] for n, h in rows])
+    sel_l = np.array([lse[n, h] for n, h in rows])
+    _gpu.assert_close(w, sel_o, sel_l, o_ref, l_ref, f"full config {cfg}")
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+class _LazyBf16:
+    """Index-on-demand float64 view of bf16 bits (avoids a full float64 copy)."""
+    def __init__(self, bits):
+        self.bits = bits
+        self.shape = bits.shape
+
+    def __getitem__(self, idx):
+        return workloads.bits_to_f64(self.bits[idx])

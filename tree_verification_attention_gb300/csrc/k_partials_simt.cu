@@ -1,0 +1,198 @@
+// k_partials_simt.cu - attention partials on the CUDA cores (float32 inputs).
+//
+// One CTA per worker of the unit decomposition in tva_common.cuh.  For every segment
+// (a contiguous run of key tiles of one row group) the CTA walks the row group in
+// blocks of 32 rows; per block it streams the segment's keys in sub-tiles of 32 and
+// keeps a running maximum / sum per row (online softmax, base 2), so each segment
+// yields the partial output O and log-sum-exp LSE of the LongSpec aggregation
+// ("Fast Tree Attention", Aggregation).  The tree tile is masked with the
+// ancestor-or-self bits of each row's node (LongSpec's tree mask; "Faster decoding",
+// "Chains and trees consume work differently").
+//
+// This path carries the float32 dtype (head_dim 64 or 128).  bfloat16 inputs go to
+// the tensor-core kernel.
+#include "tva_internal.h"
+
+namespace tva {
+namespace {
+
+constexpr int kRB = 32;       // rows per block
+constexpr int kKT = 32;       // keys per sub-tile
+constexpr int kThreads = 256; // 8 threads per row: 4 keys each for QK, D/8 columns for PV
+
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <int D>
+constexpr size_t simt_smem_bytes() {
+  return sizeof(float) * (kRB * (D + 1) + kKT * (D + 1) + kKT * D + kRB * (kKT + 1)) +
+         sizeof(uint32_t) * kMaxNodes * 4;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) {
+  extern __shared__ float smem[];
+  float* qs = smem;                          // [kRB][D+1]
+  float* ks = qs + kRB * (D + 1);            // [kKT][D+1]
+  float* vs = ks + kKT * (D + 1);            // [kKT][D]
+  float* ps = vs + kKT * D;                  // [kRB][kKT+1]
+  uint32_t* masks = reinterpret_cast<uint32_t*>(ps + kRB * (kKT + 1));  // [128][4]
+  __shared__ int tree_bad;
+
+  const Problem& pr = a.pr;
+  const T* __restrict__ q = static_cast<const T*>(a.q);
+  const int tid = threadIdx.x;
+  const int r_loc = tid >> 3;  // row of this thread inside the block
+  const int kg = tid & 7;      // key group (QK) / column phase (PV)
+  const int u = blockIdx.x;
+  const long long T_all = total_units(pr);
+  const long long c = chunk_units(pr, T_all);
+  long long t = (long long)u * c;
+  const long long t_end = min(T_all, t + c);
+  const size_t kv_stride = (size_t)pr.Hkv * D;
+
+  while (t < t_end) {
+    const Loc L = locate_unit(pr, t);
+    const long long seg_end = min(t_end, L.start + L.tiles);
+    const int tile0 = L.tile;
+    const int tile1 = (int)(seg_end - L.start);
+    const bool has_tree = tile1 == L.tiles;
+    const SeqInfo s = L.s;
+    const int slot = u + L.q;
+
+    if (has_tree) {
+      __syncthreads();
+      if (tid == 0) tree_bad = 0;
+      __syncthreads();
+      for (int i = tid; i < s.m; i += kThreads) {
+        uint32_t bits[4];
+        if (!ancestor_bits(a.parent + s.n0, i, s.m, bits)) tree_bad = 1;
+        masks[i * 4 + 0] = bits[0]; masks[i * 4 + 1] = bits[1];
+        masks[i * 4 + 2] = bits[2]; masks[i * 4 + 3] = bits[3];
+      }
+      __syncthreads();
+      if (tid == 0 && tree_bad) set_status(a.status, kStatusBadTree);
+    }
+
+    const int rows_total = s.m * pr.G;
+    const int row_begin = L.mp * pr.RG;
+    const int row_end = min(rows_total, row_begin + pr.RG);
+    for (int rb = row_begin; rb < row_end; rb += kRB) {
+      __syncthreads();
+      for (int idx = tid; idx < kRB * D; idx += kThreads) {
+        const int r = idx / D, dd = idx % D;
+        const int row = rb + r;
+        float v = 0.f;
+        if (row < row_end) {
+          const int i = row / pr.G, j = row % pr.G;
+          v = to_f(q[((size_t)(s.n0 + i) * pr.Hq + L.g * pr.G + j) * D + dd]);
+        }
+        qs[r * (D + 1) + dd] = v;
+      }
+      const int my_row = rb + r_loc;
+      const bool row_ok = my_row < row_end;
+      const int my_node = row_ok ? my_row / pr.G : 0;
+      float m_run = -INFINITY, l_run = 0.f;
+      float o[D / 8];
+#pragma unroll
+      for (int k = 0; k < D / 8; ++k) o[k] = 0.f;
+
+      for (int tile = tile0; tile < tile1; ++tile) {
+        const bool is_tree = tile == L.tiles - 1;
+        const int nkeys = is_tree ? s.m : min(kKeyTile, s.P - tile * kKeyTile);
+        const T* kb = static_cast<const T*>(is_tree ? a.tree_k : a.k_cache);
+        const T* vb = static_cast<const T*>(is_tree ? a.tree_v : a.v_cache);
+        const size_t first = is_tree ? (size_t)s.n0 : (size_t)s.p0 + (size_t)tile * kKeyTile;
+        kb += first * kv_stride + (size_t)L.g * D;
+        vb += first * kv_stride + (size_t)L.g * D;
+        for (int k0 = 0; k0 < nkeys; k0 += kKT) {
+          __syncthreads();
+          for (int idx = tid; idx < kKT * D; idx += kThreads) {
+            const int key = idx / D, dd = idx % D;
+            const bool valid = k0 + key < nkeys;
+            ks[key * (D + 1) + dd] = valid ? to_f(kb[(size_t)(k0 + key) * kv_stride + dd]) : 0.f;
+            vs[key * D + dd] = valid ? to_f(vb[(size_t)(k0 + key) * kv_stride + dd]) : 0.f;
+          }
+          __syncthreads();
+          float sc[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) sc[k] = 0.f;
+          for (int dd = 0; dd < D; ++dd) {
+            const float qv = qs[r_loc * (D + 1) + dd];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sc[k] = fmaf(qv, ks[(kg * 4 + k) * (D + 1) + dd], sc[k]);
+          }
+          float mx = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int key = k0 + kg * 4 + k;
+            bool vis = row_ok && key < nkeys;
+            if (is_tree && vis) vis = (masks[my_node * 4 + (key >> 5)] >> (key & 31)) & 1u;
+            sc[k] = vis ? sc[k] * a.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, sc[k]);
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          const float m_new = fmaxf(m_run, mx);
+          const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
+          float psum = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float p = (sc[k] == -INFINITY) ? 0.f : exp2f(sc[k] - m_new);
+            ps[r_loc * (kKT + 1) + kg * 4 + k] = p;
+            psum += p;
+          }
+          psum += __shfl_xor_sync(0xffffffffu, psum, 4);
+          psum += __shfl_xor_sync(0xffffffffu, psum, 2);
+          psum += __shfl_xor_sync(0xffffffffu, psum, 1);
+          l_run = l_run * alpha + psum;
+          m_run = m_new;
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < D / 8; ++k) o[k] *= alpha;
+          for (int j = 0; j < kKT; ++j) {
+            const float pj = ps[r_loc * (kKT + 1) + j];
+#pragma unroll
+            for (int k = 0; k < D / 8; ++k) o[k] = fmaf(pj, vs[j * D + kg + 8 * k], o[k]);
+          }
+        }
+      }
+      if (row_ok) {
+        const float inv = 1.f / l_run;
+        float* op = a.o_part + ((size_t)slot * pr.RG + (my_row - row_begin)) * D;
+#pragma unroll
+        for (int k = 0; k < D / 8; ++k) op[kg + 8 * k] = o[k] * inv;
+        if (kg == 0) a.lse_part[(size_t)slot * pr.RG + (my_row - row_begin)] = m_run + log2f(l_run);
+      }
+    }
+    t = seg_end;
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_simt_typed(const PartialArgs& a, cudaStream_t s) {
+  constexpr size_t smem = simt_smem_bytes<D>();
+  cudaError_t e = cudaFuncSetAttribute(partials_simt_kernel<T, D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  partials_simt_kernel<T, D><<<a.pr.U, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int simt_workers_per_sm() { return 3; }
+
+cudaError_t launch_partials_simt(const PartialArgs& a, int dtype, cudaStream_t s) {
+  if (dtype == 1) {
+    return a.pr.d == 64 ? launch_simt_typed<float, 64>(a, s) : launch_simt_typed<float, 128>(a, s);
+  }
+  return a.pr.d == 64 ? launch_simt_typed<__nv_bfloat16, 64>(a, s)
+                      : launch_simt_typed<__nv_bfloat16, 128>(a, s);
+}
+
+}  // namespace tva

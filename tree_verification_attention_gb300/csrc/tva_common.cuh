@@ -1,0 +1,189 @@
+// tva_common.cuh - work decomposition and small helpers shared by the kernels.
+//
+// Work decomposition ("units")
+// ----------------------------
+// Rows: for KV head g of sequence b, the m_b * G query rows (node i, query head
+// g*G + j) are numbered r = i*G + j and cut into row groups of RG = 128 * W rows.
+// Keys: each row group sees the P_b prefix keys, cut into tiles of 128, plus ONE more
+// tile holding the sequence's tree keys (masked to ancestors-and-self).
+// A unit is one (row group, key tile) pair.  Units are numbered sequence by sequence,
+// KV head by KV head, row group by row group, tile by tile (the tree tile last).  The
+// U workers (CTAs) take equal contiguous ranges of c = ceil(T / U) units, so a
+// worker's range can cross row-group boundaries; each maximal piece of a range inside
+// one row group is a "segment" and produces one partial (O, LSE) per row.  The
+// segment of worker u in row group q is stored in slot u + q: distinct pieces never
+// share a slot, because worker u+1 starting inside group q-1 would contradict worker
+// u reaching group q.  Partials therefore need at most U + Q slots (Q row groups).
+//
+// Both the partials kernels and the combine kernel recompute this map from
+// cu_prefix / cu_nodes, so no schedule table is stored.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace tva {
+
+constexpr int kKeyTile = 128;   // keys per unit
+constexpr int kMaxNodes = 128;  // tree nodes per sequence (ancestor mask = 4 words)
+
+enum : int {
+  kStatusOk = 0,
+  kStatusInvalidArg = 1,
+  kStatusBadTree = 3,
+  kStatusTimeout = 6,
+};
+
+struct Problem {
+  const int32_t* cu_prefix;  // null: single sequence of single_prefix keys
+  const int32_t* cu_nodes;   // null: single sequence of single_nodes nodes
+  int single_prefix, single_nodes;
+  int B, Hq, Hkv, G, d;
+  int RG;                    // rows per row group
+  int U;                     // workers
+  int max_prefix, max_nodes, kv_capacity, node_capacity;
+};
+
+struct SeqInfo {
+  int p0, P;   // first k_cache row, prefix length
+  int n0, m;   // first node row, tree size
+  bool ok;     // false: bounds violated (sequence treated as empty)
+};
+
+__device__ __forceinline__ void set_status(int32_t* st, int code) {
+  if (st != nullptr) atomicCAS(reinterpret_cast<int*>(st), 0, code);
+}
+
+__device__ __forceinline__ SeqInfo seq_info(const Problem& pr, int b) {
+  SeqInfo s;
+  if (pr.cu_prefix == nullptr) {
+    s.p0 = 0; s.P = pr.single_prefix; s.n0 = 0; s.m = pr.single_nodes;
+  } else {
+    s.p0 = __ldg(pr.cu_prefix + b);
+    s.P = __ldg(pr.cu_prefix + b + 1) - s.p0;
+    s.n0 = __ldg(pr.cu_nodes + b);
+    s.m = __ldg(pr.cu_nodes + b + 1) - s.n0;
+  }
+  s.ok = s.p0 >= 0 && s.P >= 0 && s.P <= pr.max_prefix && s.p0 + s.P <= pr.kv_capacity &&
+         s.n0 >= 0 && s.m >= 0 && s.m <= pr.max_nodes && s.n0 + s.m <= pr.node_capacity;
+  if (!s.ok) { s.P = 0; s.m = 0; }
+  return s;
+}
+
+__device__ __forceinline__ int seq_tiles(int P) { return (P + kKeyTile - 1) / kKeyTile + 1; }
+__device__ __forceinline__ int seq_groups(const Problem& pr, int m) {
+  return (m * pr.G + pr.RG - 1) / pr.RG;
+}
+
+// Total units T and the chunk size c = ceil(T / U).
+__device__ __forceinline__ long long total_units(const Problem& pr) {
+  long long T = 0;
+  for (int b = 0; b < pr.B; ++b) {
+    SeqInfo s = seq_info(pr, b);
+    T += (long long)pr.Hkv * seq_groups(pr, s.m) * seq_tiles(s.P);
+  }
+  return T;
+}
+
+__device__ __forceinline__ long long chunk_units(const Problem& pr, long long T) {
+  return (T + pr.U - 1) / pr.U;
+}
+
+// Where unit t lives.
+struct Loc {
+  SeqInfo s;
+  int b;
+  int g, mp;          // KV head, row group within (b, g)
+  int MP;             // row groups per (b, g)
+  int tiles;          // units per row group (prefix tiles + 1 tree tile)
+  int tile;           // tile index of unit t inside its row group
+  int q;              // global row-group index
+  long long start;    // global index of the row group's first unit
+};
+
+__device__ __forceinline__ Loc locate_unit(const Problem& pr, long long t) {
+  Loc L;
+  long long acc = 0;
+  int qacc = 0;
+  for (int b = 0; b < pr.B; ++b) {
+    SeqInfo s = seq_info(pr, b);
+    int MP = seq_groups(pr, s.m);
+    int tiles = seq_tiles(s.P);
+    long long units = (long long)pr.Hkv * MP * tiles;
+    if (t < acc + units) {
+      long long local = t - acc;
+      int gi = (int)(local / tiles);
+      L.s = s; L.b = b; L.MP = MP; L.tiles = tiles;
+      L.g = gi / MP; L.mp = gi % MP;
+      L.tile = (int)(local % tiles);
+      L.q = qacc + gi;
+      L.start = acc + (long long)gi * tiles;
+      return L;
+    }
+    acc += units;
+    qacc += pr.Hkv * MP;
+  }
+  L.b = -1;  // not reached for t < T
+  return L;
+}
+
+// Row group of query row (node n, head h), for the combine.
+struct RowLoc {
+  SeqInfo s;
+  int b, q, r;        // sequence, global row group, row inside the group
+  int tiles;
+  long long start;    // first unit of the row group
+  long long T;        // total units
+};
+
+__device__ __forceinline__ bool locate_row(const Problem& pr, int n, int h, RowLoc& R) {
+  long long acc = 0;
+  int qacc = 0;
+  bool found = false;
+  for (int b = 0; b < pr.B; ++b) {
+    SeqInfo s = seq_info(pr, b);
+    int MP = seq_groups(pr, s.m);
+    int tiles = seq_tiles(s.P);
+    if (!found && n >= s.n0 && n < s.n0 + s.m) {
+      int g = h / pr.G, j = h % pr.G;
+      int rs = (n - s.n0) * pr.G + j;
+      int mp = rs / pr.RG;
+      R.s = s; R.b = b; R.r = rs % pr.RG; R.tiles = tiles;
+      R.q = qacc + g * MP + mp;
+      R.start = acc + (long long)(g * MP + mp) * tiles;
+      found = true;
+    }
+    acc += (long long)pr.Hkv * MP * tiles;
+    qacc += pr.Hkv * MP;
+  }
+  R.T = acc;
+  return found;
+}
+
+// Ancestor-or-self bit mask of tree node i (local id) over local ids 0..127:
+// mask bit c set iff node c is i or an ancestor of i.  Returns false if a parent id
+// met on the walk is outside [-1, node) (then only i's own bit is set).
+__device__ __forceinline__ bool ancestor_bits(const int32_t* parent_seq, int i, int m,
+                                              uint32_t bits[4]) {
+  bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+  bits[i >> 5] |= 1u << (i & 31);
+  int j = i;
+  for (int steps = 0; steps < kMaxNodes; ++steps) {
+    int p = __ldg(parent_seq + j);
+    if (p < -1 || p >= j || p >= m) {
+      bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+      bits[i >> 5] |= 1u << (i & 31);
+      return false;
+    }
+    if (p < 0) return true;
+    bits[p >> 5] |= 1u << (p & 31);
+    j = p;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+}  // namespace tva

@@ -1,0 +1,320 @@
+// tva_host.cu - the C ABI (include/tva.h): argument checks, workspace layout and
+// kernel launches.  No torch types cross this boundary.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "tva.h"
+#include "tva_internal.h"
+
+namespace {
+
+using tva::Problem;
+
+constexpr int kMaxDevices = 64;
+
+int device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  static int cache[kMaxDevices] = {0};
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return -1;
+    cache[dev] = v;
+  }
+  *sms = cache[dev];
+  return 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Host-side shape checks shared by every attention entry point.
+tva_status check_shape(int B, int Hq, int Hkv, int d, int dtype, int max_prefix, int max_nodes,
+                       long long kv_cap, long long node_cap) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return TVA_ERR_INVALID_ARG;
+  if (max_prefix < 0 || max_nodes < 1 || kv_cap < 0 || node_cap < 0) return TVA_ERR_INVALID_ARG;
+  if (max_nodes > tva::kMaxNodes) return TVA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return TVA_ERR_UNSUPPORTED;
+  if (dtype != TVA_BF16 && dtype != TVA_FP32) return TVA_ERR_UNSUPPORTED;
+  // index arithmetic inside the kernels is 32-bit for row counts
+  if (kv_cap > (1LL << 31) - 1 - tva::kKeyTile || node_cap > (1LL << 24)) return TVA_ERR_INVALID_ARG;
+  if ((long long)B * max_nodes > (1LL << 24) || (long long)B * max_prefix > (1LL << 40))
+    return TVA_ERR_INVALID_ARG;
+  return TVA_OK;
+}
+
+struct Layout {
+  Problem pr;
+  size_t o_bytes, lse_bytes, total;
+  long long slots;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Fills the device-visible problem and the workspace layout.  cu_* may be null for
+// the single-sequence form.
+tva_status make_layout(int B, int Hq, int Hkv, int d, int dtype, int max_prefix, int max_nodes,
+                       int kv_cap, int node_cap, const int32_t* cu_prefix, const int32_t* cu_nodes,
+                       int single_prefix, int single_nodes, Layout* L) {
+  tva_status st = check_shape(B, Hq, Hkv, d, dtype, max_prefix, max_nodes, kv_cap, node_cap);
+  if (st != TVA_OK) return st;
+  int sms = 0;
+  if (device_sms(&sms) != 0) return TVA_ERR_CUDA;
+  const int G = Hq / Hkv;
+  const int W = (max_nodes * G > 128) ? 2 : 1;
+  Problem& pr = L->pr;
+  pr.cu_prefix = cu_prefix;
+  pr.cu_nodes = cu_nodes;
+  pr.single_prefix = single_prefix;
+  pr.single_nodes = single_nodes;
+  pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.G = G; pr.d = d;
+  pr.RG = 128 * W;
+  pr.U = sms * tva::simt_workers_per_sm();
+  pr.max_prefix = max_prefix; pr.max_nodes = max_nodes;
+  pr.kv_capacity = kv_cap; pr.node_capacity = node_cap;
+  const long long groups = (long long)B * Hkv * ((max_nodes * G + pr.RG - 1) / pr.RG);
+  L->slots = pr.U + groups;
+  L->o_bytes = align256((size_t)L->slots * pr.RG * d * sizeof(float));
+  L->lse_bytes = align256((size_t)L->slots * pr.RG * sizeof(float));
+  L->total = L->o_bytes + L->lse_bytes;
+  return TVA_OK;
+}
+
+tva_status layout_from_params(const tva_params* p, Layout* L) {
+  if (p == nullptr) return TVA_ERR_INVALID_ARG;
+  return make_layout(p->batch, p->num_q_heads, p->num_kv_heads, p->head_dim, (int)p->dtype,
+                     p->max_prefix_len, p->max_nodes, p->kv_capacity, p->node_capacity,
+                     p->cu_prefix, p->cu_nodes, 0, 0, L);
+}
+
+float scale_log2(float softmax_scale, int d) {
+  const float s = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)d);
+  return s * 1.44269504088896340736f;
+}
+
+tva_status run_partials(const Layout& L, int dtype, float softmax_scale, const void* q,
+                        const void* k_cache, const void* v_cache, const void* tree_k,
+                        const void* tree_v, const int32_t* parent, void* workspace,
+                        int32_t* dev_status, cudaStream_t s) {
+  tva::PartialArgs a;
+  a.pr = L.pr;
+  a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.tree_k = tree_k; a.tree_v = tree_v;
+  a.parent = parent;
+  a.scale_log2 = scale_log2(softmax_scale, L.pr.d);
+  a.o_part = static_cast<float*>(workspace);
+  a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.o_bytes);
+  a.status = dev_status;
+  return tva::launch_partials_simt(a, dtype, s) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
+}
+
+tva_status run_combine(const Layout& L, int dtype, const void* workspace, void* out, float* lse,
+                       int32_t* dev_status, cudaStream_t s) {
+  tva::CombineArgs a;
+  a.pr = L.pr;
+  a.o_part = static_cast<const float*>(workspace);
+  a.lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + L.o_bytes);
+  a.out = out; a.lse = lse; a.status = dev_status;
+  return tva::launch_combine(a, dtype, s) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
+}
+
+tva_status check_io_ptrs(const void* q, const void* k_cache, const void* v_cache,
+                         const void* tree_k, const void* tree_v, const int32_t* parent,
+                         long long kv_cap) {
+  if (!q || !tree_k || !tree_v || !parent) return TVA_ERR_INVALID_ARG;
+  if (kv_cap > 0 && (!k_cache || !v_cache)) return TVA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(tree_k) ||
+      !aligned16(tree_v))
+    return TVA_ERR_INVALID_ARG;
+  return TVA_OK;
+}
+
+tva_status check_workspace(const Layout& L, const void* ws, size_t bytes) {
+  if (ws == nullptr || bytes < L.total) return TVA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return TVA_ERR_WORKSPACE;
+  return TVA_OK;
+}
+
+// ---- convenience-form state (library-owned, per device) ----
+struct OwnedState {
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  int32_t* status = nullptr;
+};
+std::mutex g_owned_mu;
+OwnedState g_owned[kMaxDevices];
+
+}  // namespace
+
+extern "C" {
+
+const char* tva_status_string(tva_status s) {
+  switch (s) {
+    case TVA_OK: return "TVA_OK";
+    case TVA_ERR_INVALID_ARG: return "TVA_ERR_INVALID_ARG";
+    case TVA_ERR_UNSUPPORTED: return "TVA_ERR_UNSUPPORTED";
+    case TVA_ERR_BAD_TREE: return "TVA_ERR_BAD_TREE";
+    case TVA_ERR_WORKSPACE: return "TVA_ERR_WORKSPACE";
+    case TVA_ERR_CUDA: return "TVA_ERR_CUDA";
+    case TVA_ERR_TIMEOUT: return "TVA_ERR_TIMEOUT";
+  }
+  return "TVA_ERR_UNKNOWN";
+}
+
+size_t tva_workspace_size(const tva_params* p) {
+  Layout L;
+  if (layout_from_params(p, &L) != TVA_OK) return 0;
+  return L.total;
+}
+
+int tva_num_workers(const tva_params* p) {
+  Layout L;
+  if (layout_from_params(p, &L) != TVA_OK) return -1;
+  return L.pr.U;
+}
+
+tva_status tree_verify_attn_partials(const tva_params* p, const void* q, const void* k_cache,
+                                     const void* v_cache, const void* tree_k,
+                                     const void* tree_v, const int32_t* parent,
+                                     void* workspace, size_t workspace_bytes,
+                                     int32_t* dev_status, void* stream) {
+  if (p == nullptr || p->cu_prefix == nullptr || p->cu_nodes == nullptr || dev_status == nullptr)
+    return TVA_ERR_INVALID_ARG;
+  tva_status st = check_shape(p->batch, p->num_q_heads, p->num_kv_heads, p->head_dim,
+                              (int)p->dtype, p->max_prefix_len, p->max_nodes, p->kv_capacity,
+                              p->node_capacity);
+  if (st != TVA_OK) return st;
+  st = check_io_ptrs(q, k_cache, v_cache, tree_k, tree_v, parent, p->kv_capacity);
+  if (st != TVA_OK) return st;
+  Layout L;
+  st = layout_from_params(p, &L);
+  if (st != TVA_OK) return st;
+  st = check_workspace(L, workspace, workspace_bytes);
+  if (st != TVA_OK) return st;
+  return run_partials(L, (int)p->dtype, p->softmax_scale, q, k_cache, v_cache, tree_k, tree_v,
+                      parent, workspace, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+tva_status tree_verify_attn_combine(const tva_params* p, const void* workspace,
+                                    size_t workspace_bytes, void* out, float* lse,
+                                    int32_t* dev_status, void* stream) {
+  if (p == nullptr || p->cu_prefix == nullptr || p->cu_nodes == nullptr || dev_status == nullptr)
+    return TVA_ERR_INVALID_ARG;
+  if (out == nullptr || lse == nullptr || !aligned16(out)) return TVA_ERR_INVALID_ARG;
+  Layout L;
+  tva_status st = layout_from_params(p, &L);
+  if (st != TVA_OK) return st;
+  st = check_workspace(L, workspace, workspace_bytes);
+  if (st != TVA_OK) return st;
+  return run_combine(L, (int)p->dtype, workspace, out, lse, dev_status,
+                     static_cast<cudaStream_t>(stream));
+}
+
+tva_status tree_verify_attn_varlen(const tva_params* p, const void* q, const void* k_cache,
+                                   const void* v_cache, const void* tree_k,
+                                   const void* tree_v, const int32_t* parent, void* out,
+                                   float* lse, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, void* stream) {
+  if (out == nullptr || lse == nullptr || !aligned16(out)) return TVA_ERR_INVALID_ARG;
+  tva_status st = tree_verify_attn_partials(p, q, k_cache, v_cache, tree_k, tree_v, parent,
+                                            workspace, workspace_bytes, dev_status, stream);
+  if (st != TVA_OK) return st;
+  return tree_verify_attn_combine(p, workspace, workspace_bytes, out, lse, dev_status, stream);
+}
+
+tva_status tree_verify_attn(const void* q, const void* k_cache, const void* v_cache,
+                            int prefix_len, const void* tree_k, const void* tree_v,
+                            const int32_t* parent, int num_nodes, int num_q_heads,
+                            int num_kv_heads, int head_dim, tva_dtype dtype, void* out,
+                            float* lse, void* stream) {
+  if (prefix_len < 0 || num_nodes < 1) return TVA_ERR_INVALID_ARG;
+  if (out == nullptr || lse == nullptr || !aligned16(out)) return TVA_ERR_INVALID_ARG;
+  tva_status st = check_io_ptrs(q, k_cache, v_cache, tree_k, tree_v, parent, prefix_len);
+  if (st != TVA_OK) return st;
+  Layout L;
+  st = make_layout(1, num_q_heads, num_kv_heads, head_dim, (int)dtype, prefix_len, num_nodes,
+                   prefix_len, num_nodes, nullptr, nullptr, prefix_len, num_nodes, &L);
+  if (st != TVA_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TVA_ERR_CUDA;
+  void* ws = nullptr;
+  int32_t* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_owned_mu);
+    OwnedState& o = g_owned[dev];
+    if (o.status == nullptr) {
+      if (cudaMalloc(&o.status, sizeof(int32_t)) != cudaSuccess) return TVA_ERR_CUDA;
+      if (cudaMemset(o.status, 0, sizeof(int32_t)) != cudaSuccess) return TVA_ERR_CUDA;
+    }
+    if (o.ws_bytes < L.total) {
+      if (o.ws != nullptr) {
+        cudaDeviceSynchronize();  // the old buffer may still be in use by queued work
+        cudaFree(o.ws);
+        o.ws = nullptr;
+        o.ws_bytes = 0;
+      }
+      if (cudaMalloc(&o.ws, L.total) != cudaSuccess) return TVA_ERR_CUDA;
+      o.ws_bytes = L.total;
+    }
+    ws = o.ws;
+    status = o.status;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_partials(L, (int)dtype, 0.f, q, k_cache, v_cache, tree_k, tree_v, parent, ws, status, s);
+  if (st != TVA_OK) return st;
+  return run_combine(L, (int)dtype, ws, out, lse, status, s);
+}
+
+tva_status tva_read_device_status(int32_t* host_status, void* stream) {
+  if (host_status == nullptr) return TVA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TVA_ERR_CUDA;
+  int32_t* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_owned_mu);
+    status = g_owned[dev].status;
+  }
+  *host_status = 0;
+  if (status == nullptr) return TVA_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_status, status, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return TVA_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return TVA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return TVA_ERR_CUDA;
+  return TVA_OK;
+}
+
+void tva_release(void) {
+  std::lock_guard<std::mutex> lock(g_owned_mu);
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return;
+  for (int dev = 0; dev < kMaxDevices; ++dev) {
+    OwnedState& o = g_owned[dev];
+    if (o.ws == nullptr && o.status == nullptr) continue;
+    if (cudaSetDevice(dev) != cudaSuccess) continue;
+    cudaDeviceSynchronize();
+    if (o.ws) cudaFree(o.ws);
+    if (o.status) cudaFree(o.status);
+    o = OwnedState();
+  }
+  cudaSetDevice(prev);
+}
+
+tva_status accept_longest_path(int batch, int node_capacity, const int32_t* cu_nodes,
+                               const int32_t* parent,
+                               const int32_t* draft_tok, const int32_t* target_argmax,
+                               int32_t* accept_len, int32_t* accept_path, int32_t* next_token,
+                               int32_t* dev_status, void* stream) {
+  if (batch < 1 || node_capacity < 0 || !cu_nodes || !parent || !draft_tok || !target_argmax || !accept_len ||
+      !accept_path || !next_token || !dev_status)
+    return TVA_ERR_INVALID_ARG;
+  tva::AcceptArgs a;
+  a.B = batch; a.node_capacity = node_capacity; a.cu_nodes = cu_nodes; a.parent = parent; a.draft_tok = draft_tok;
+  a.target_argmax = target_argmax; a.accept_len = accept_len; a.accept_path = accept_path;
+  a.next_token = next_token; a.status = dev_status;
+  return tva::launch_accept(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TVA_OK
+                                                                                 : TVA_ERR_CUDA;
+}
+
+}  // extern "C"

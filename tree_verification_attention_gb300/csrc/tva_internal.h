@@ -1,0 +1,54 @@
+// tva_internal.h - launch interface between the C-ABI host code and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "tva_common.cuh"
+
+namespace tva {
+
+struct PartialArgs {
+  Problem pr;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const void* tree_k;
+  const void* tree_v;
+  const int32_t* parent;
+  float scale_log2;   // softmax_scale * log2(e): logits are kept in base 2
+  float* o_part;      // [slots][RG][d] normalised partial outputs
+  float* lse_part;    // [slots][RG] partial log2-sum-exp2 of the base-2 logits
+  int32_t* status;
+};
+
+struct CombineArgs {
+  Problem pr;
+  const float* o_part;
+  const float* lse_part;
+  void* out;
+  float* lse;
+  int32_t* status;
+};
+
+struct AcceptArgs {
+  int B;
+  int node_capacity;
+  const int32_t* cu_nodes;
+  const int32_t* parent;
+  const int32_t* draft_tok;
+  const int32_t* target_argmax;
+  int32_t* accept_len;
+  int32_t* accept_path;
+  int32_t* next_token;
+  int32_t* status;
+};
+
+// dtype: 0 = bf16, 1 = fp32 (tva_dtype values)
+int simt_workers_per_sm();
+cudaError_t launch_partials_simt(const PartialArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
+
+}  // namespace tva

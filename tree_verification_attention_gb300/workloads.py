@@ -64,8 +64,9 @@ def bf16_round_bits(x: np.ndarray) -> np.ndarray:
 
     Inputs are finite Gaussian draws, so NaN handling is not needed."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = x.view(np.uint32)
+    # finite inputs stay below 0xFF800000 after the increment, so uint32 cannot wrap
+    rounded = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return rounded.astype(np.uint16)
 
 
