@@ -163,6 +163,11 @@ tva_status accept_longest_path(int batch, int node_capacity, const int32_t* cu_n
                                int32_t* accept_len, int32_t* accept_path,
                                int32_t* next_token, int32_t* dev_status, void* stream);
 
+/* Description of the last host-side CUDA or driver failure seen by this thread
+ * (the call that failed and its error string), "" if none.  Thread-local storage,
+ * valid until the thread's next failing call. */
+const char* tva_last_error(void);
+
 /* Human-readable name of a status code (static storage). */
 const char* tva_status_string(tva_status s);
 

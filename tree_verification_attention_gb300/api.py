@@ -70,6 +70,7 @@ def load_library(path: str | None = None):
         "tva_release": (None, []),
         "accept_longest_path": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "tva_status_string": (ctypes.c_char_p, [_I]),
+        "tva_last_error": (ctypes.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -85,7 +86,8 @@ def status_string(code: int) -> str:
 
 def _check(code: int, where: str):
     if code != 0:
-        raise TvaError(code, where)
+        detail = load_library().tva_last_error().decode() if code == 5 else ""
+        raise TvaError(code, where + (f" [{detail}]" if detail else ""))
 
 
 def _ptr(t):

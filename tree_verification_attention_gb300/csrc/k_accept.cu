@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
   if (a.B <= 0) return cudaSuccess;
   accept_kernel<<<(a.B + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return check_cuda(cudaGetLastError(), "launch accept_kernel");
 }
 
 }  // namespace tva

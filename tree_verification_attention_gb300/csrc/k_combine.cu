@@ -76,7 +76,7 @@ cudaError_t launch_typed(const CombineArgs& a, cudaStream_t s) {
   const long long blocks = (rows + 7) / 8;
   if (blocks <= 0) return cudaSuccess;
   combine_kernel<T, D><<<(unsigned)blocks, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return check_cuda(cudaGetLastError(), "launch combine_kernel");
 }
 
 }  // namespace

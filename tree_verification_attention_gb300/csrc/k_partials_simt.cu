@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
   const int r_loc = tid >> 3;  // row of this thread inside the block
   const int kg = tid & 7;      // key group (QK) / column phase (PV)
   const int u = blockIdx.x;
+  if (u == 0 && tid == 0) validate_sequences(pr, a.status);
   const long long T_all = total_units(pr);
   const long long c = chunk_units(pr, T_all);
   long long t = (long long)u * c;
@@ -176,11 +177,12 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
 template <typename T, int D>
 cudaError_t launch_simt_typed(const PartialArgs& a, cudaStream_t s) {
   constexpr size_t smem = simt_smem_bytes<D>();
-  cudaError_t e = cudaFuncSetAttribute(partials_simt_kernel<T, D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = check_cuda(cudaFuncSetAttribute(partials_simt_kernel<T, D>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                             "cudaFuncSetAttribute(partials_simt_kernel)");
   if (e != cudaSuccess) return e;
   partials_simt_kernel<T, D><<<a.pr.U, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return check_cuda(cudaGetLastError(), "launch partials_simt_kernel");
 }
 
 }  // namespace
@@ -188,11 +190,11 @@ cudaError_t launch_simt_typed(const PartialArgs& a, cudaStream_t s) {
 int simt_workers_per_sm() { return 3; }
 
 cudaError_t launch_partials_simt(const PartialArgs& a, int dtype, cudaStream_t s) {
-  if (dtype == 1) {
-    return a.pr.d == 64 ? launch_simt_typed<float, 64>(a, s) : launch_simt_typed<float, 128>(a, s);
+  if (dtype != 1) {  // bf16 runs on the tensor-core kernel
+    record_error("launch_partials_simt", 0, "float32 only");
+    return cudaErrorInvalidValue;
   }
-  return a.pr.d == 64 ? launch_simt_typed<__nv_bfloat16, 64>(a, s)
-                      : launch_simt_typed<__nv_bfloat16, 128>(a, s);
+  return a.pr.d == 64 ? launch_simt_typed<float, 64>(a, s) : launch_simt_typed<float, 128>(a, s);
 }
 
 }  // namespace tva

@@ -1,0 +1,618 @@
+// k_partials_tc.cu - attention partials on the 5th-generation tensor cores (bf16).
+//
+// What is computed: for every segment of the unit decomposition (tva_common.cuh), the
+// partial output O and log-sum-exp LSE of the segment's key tiles, per query row -
+// the O_cache / O_specs, LSE_cache / LSE_specs of LongSpec's Hybrid Tree Attention
+// ("Fast Tree Attention": cached pairs need no mask; the speculative pairs are masked
+// by the tree, each node seeing its ancestors and itself).  The tree keys are simply
+// one more 128-key tile whose logits are masked with the row's ancestor bits.
+//
+// How (one CTA per SM, 320 threads):
+//   warp 8  (producer): TMA loads of Q (once per segment) and of the K / V tiles into
+//           a ring of shared-memory stages, 128-byte swizzled.
+//   warp 9  (MMA):      single-thread tcgen05.mma issue.  S = Q K^T (both operands in
+//           shared memory) into TMEM; O += P V with P read from TMEM (P overwrites
+//           the first half of its S buffer as packed bf16) and V from shared memory.
+//   warps 0-7 (softmax): two streams of 4 warps; thread r of a stream owns TMEM lane
+//           (= query row) r, so row max / sum need no shuffles.  A stream's running
+//           max is only moved when it grows by more than 2^8 (stale maxima cancel in
+//           the final division), and then O is rescaled in TMEM.
+// Streams: with 2 M-tiles per row group (W = 2) stream w owns M-tile w and sees every
+// key tile; with W = 1 both streams share the M-tile and take alternate key tiles,
+// and their two partials are merged in the epilogue.  Either way the MMA warp issues
+//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ...
+// so each stream's softmax overlaps the other stream's MMAs, and the commit that
+// publishes S_w(j+1) also covers PV_w(j): a stream may rescale its O right after its
+// S is ready.
+// TMEM columns: S/P buffers at 0 and 128, O accumulators at 256 and 384 (512 total).
+//
+// Every wait is bounded (2 s): on expiry the CTA raises an abort flag, records
+// TVA_ERR_TIMEOUT, drains its in-flight copies and MMAs (bounded again), frees TMEM
+// and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+
+#include "tc_ptx.cuh"
+#include "tva_internal.h"
+
+namespace tva {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreadsTc = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr int kHalfBytes = 128 * 128;  // 128 rows of 64 bf16 (one 128-byte swizzle span)
+constexpr uint32_t kNegInfBits = 0xff800000u;
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kQBytes = 2 * kHalves * kHalfBytes;
+  static constexpr int kBarOff = kQBytes + kStages * kTileBytes;
+  static constexpr int kMiscBytes = 4096;
+  static constexpr int kSmemBytes = kBarOff + kMiscBytes + 1024;  // + alignment slack
+};
+
+struct TcArgs {
+  PartialArgs a;
+  int W;    // M-tiles per row group (1 or 2)
+  int npt;  // nodes per M-tile: floor(128 / G)
+};
+
+struct Segment {
+  Loc L;
+  int tile0, n;
+};
+
+__device__ __forceinline__ bool next_segment(const Problem& pr, long long& t, long long t_end,
+                                             Segment& s) {
+  if (t >= t_end) return false;
+  s.L = locate_unit(pr, t);
+  const long long seg_end = min(t_end, s.L.start + s.L.tiles);
+  s.tile0 = s.L.tile;
+  s.n = (int)(seg_end - t);
+  t = seg_end;
+  return true;
+}
+
+// Logits of keys c0 .. c0+63 that the row does not see become -inf: keys at or past
+// `lim`, and in the tree tile keys that are not the row's node or its ancestors.
+__device__ __forceinline__ void mask64(uint32_t* s, int c0, int lim, bool is_tree, bool row_ok,
+                                       const uint32_t* anc) {
+#pragma unroll
+  for (int e = 0; e < 64; ++e) {
+    const int c = c0 + e;
+    bool vis = c < lim;
+    if (is_tree) vis = vis && row_ok && ((anc[c >> 5] >> (c & 31)) & 1u);
+    if (!vis) s[e] = kNegInfBits;
+  }
+}
+
+// Waits that ignore the abort flag (used only while draining).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  volatile int never = 0;
+  mbar_wait(bar, parity, &never, kWaitNs);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsTc, 1)
+    partials_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_tk,
+                       const __grid_constant__ CUtensorMap tm_tv, const TcArgs args) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const PartialArgs& a = args.a;
+  const Problem& pr = a.pr;
+  const int W = args.W, npt = args.npt, G = pr.G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x;
+
+  if (u == 0 && threadIdx.x == 0) validate_sequences(pr, a.status);
+  const long long T_all = total_units(pr);
+  const long long chunk = chunk_units(pr, T_all);
+  const long long t_begin = (long long)u * chunk;
+  const long long t_end = min(T_all, t_begin + chunk);
+  if (t_begin >= t_end) return;  // uniform over the CTA
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t q_s = sbase;
+  const uint32_t kv_s = sbase + C::kQBytes;
+  const uint32_t bar0 = sbase + C::kBarOff;
+  const uint32_t KV_FULL = bar0;                        // [kStages]
+  const uint32_t KV_EMPTY = bar0 + 8 * C::kStages;      // [kStages]
+  const uint32_t Q_FULL = bar0 + 16 * C::kStages;
+  const uint32_t Q_EMPTY = Q_FULL + 8;
+  const uint32_t S_FULL = Q_EMPTY + 8;                  // [2]
+  const uint32_t P_FULL = S_FULL + 16;                  // [2]
+  const uint32_t O_FULL = P_FULL + 16;                  // [2]
+  const uint32_t O_FREE = O_FULL + 16;
+  const uint32_t M1_READY = O_FREE + 8;
+  const uint32_t DRAIN = M1_READY + 8;
+  uint8_t* misc = smem + C::kBarOff + 16 * C::kStages + 8 * 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  float* m1_s = reinterpret_cast<float*>(smem + C::kBarOff + 512);  // [2][128]
+  float* l1_s = m1_s + 256;                                         // [2][128]
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(KV_FULL + 8 * s, 1);
+      mbar_init(KV_EMPTY + 8 * s, 1);
+    }
+    mbar_init(Q_FULL, 1);
+    mbar_init(Q_EMPTY, 1);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(S_FULL + 8 * w, 1);
+      mbar_init(P_FULL + 8 * w, 128);
+      mbar_init(O_FULL + 8 * w, 1);
+    }
+    mbar_init(O_FREE, 256);
+    mbar_init(M1_READY, 128);
+    mbar_init(DRAIN, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_tk);
+      prefetch_tmap(&tm_tv);
+      int ring = 0, sg = 0;
+      bool ok = true;
+      long long t = t_begin;
+      Segment S;
+      const uint32_t q_box_bytes = 64u * G * npt * 2u;
+      while (ok && next_segment(pr, t, t_end, S)) {
+        const Loc& L = S.L;
+        if (sg > 0 && !mbar_wait(Q_EMPTY, (sg - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        mbar_expect_tx(Q_FULL, (uint32_t)W * C::kHalves * q_box_bytes);
+        for (int mt = 0; mt < W; ++mt)
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(q_s + (mt * C::kHalves + h) * kHalfBytes, &tm_q, 64 * h, L.g * G,
+                        L.s.n0 + (L.mp * W + mt) * npt, Q_FULL);
+        auto load = [&](int k, bool is_v) -> bool {
+          const int stage = ring % C::kStages, use = ring / C::kStages;
+          if (use > 0 && !mbar_wait(KV_EMPTY + 8 * stage, (use - 1) & 1, abort_flag, kWaitNs))
+            return false;
+          const int tile = S.tile0 + k;
+          const bool tree = tile == L.tiles - 1;
+          const CUtensorMap* m = tree ? (is_v ? &tm_tv : &tm_tk) : (is_v ? &tm_v : &tm_k);
+          const int z = tree ? L.s.n0 : L.s.p0 + tile * kKeyTile;
+          mbar_expect_tx(KV_FULL + 8 * stage, C::kTileBytes);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(kv_s + stage * C::kTileBytes + h * kHalfBytes, m, 64 * h, L.g, z,
+                        KV_FULL + 8 * stage);
+          ++ring;
+          return true;
+        };
+        const int n = S.n;
+        if (W == 2) {
+          for (int k = 0; k < n && ok; ++k) ok = load(k, false) && load(k, true);
+        } else {
+          ok = load(0, false);
+          if (ok && n > 1) ok = load(1, false);
+          for (int j = 0; j < n && ok; ++j) {
+            ok = load(j, true);
+            if (ok && j + 2 < n) ok = load(j + 2, false);
+          }
+        }
+        ++sg;
+      }
+      // drain: every copy this thread started has landed before TMEM / smem go away
+      for (int i = max(0, ring - C::kStages); i < ring; ++i)
+        drain_wait(KV_FULL + 8 * (i % C::kStages), (i / C::kStages) & 1);
+      if (sg > 0) drain_wait(Q_FULL, (sg - 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false);
+      constexpr uint32_t idesc_o = idesc_bf16(128, D, true);
+      int ring = 0, sg = 0;
+      uint32_t pbits = 0;  // bit w: parity of the next P_FULL[w] phase
+      bool ok = true;
+      long long t = t_begin;
+      Segment S;
+      auto wait_kv = [&](int idx) -> bool {
+        if (!mbar_wait(KV_FULL + 8 * (idx % C::kStages), (idx / C::kStages) & 1, abort_flag, kWaitNs))
+          return false;
+        tc_fence_after();
+        return true;
+      };
+      auto issue_s = [&](int w, int mt, int idx) {
+        const uint32_t kb = kv_s + (idx % C::kStages) * C::kTileBytes;
+        const uint32_t qb = q_s + mt * C::kHalves * kHalfBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+          mma_ss(tmem + w * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                 idesc_s, ks > 0);
+        }
+        tc_commit(S_FULL + 8 * w);
+      };
+      auto issue_pv = [&](int w, int idx, bool acc) {
+        const uint32_t vb = kv_s + (idx % C::kStages) * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < kKeyTile / 16; ++ks)
+          mma_ts(tmem + 256 + w * 128, tmem + w * 128 + ks * 8,
+                 sdesc_sw128(vb + ks * 2048, kHalfBytes, 1024), idesc_o, (acc || ks > 0) ? 1u : 0u);
+      };
+      auto wait_p = [&](int w) -> bool {
+        if (!mbar_wait(P_FULL + 8 * w, (pbits >> w) & 1u, abort_flag, kWaitNs)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto wait_ofree = [&]() -> bool {
+        if (sg == 0) return true;
+        if (!mbar_wait(O_FREE, (sg - 1) & 1, abort_flag, kWaitNs)) return false;
+        tc_fence_after();
+        return true;
+      };
+      while (ok && next_segment(pr, t, t_end, S)) {
+        const int n = S.n;
+        if (!mbar_wait(Q_FULL, sg & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        tc_fence_after();
+        if (W == 2) {
+          // ring: K_k at ring + 2k, V_k at ring + 2k + 1
+          if (!(ok = wait_kv(ring))) break;
+          issue_s(0, 0, ring);
+          issue_s(1, 1, ring);
+          tc_commit(KV_EMPTY + 8 * (ring % C::kStages));
+          if (n == 1) tc_commit(Q_EMPTY);
+          for (int k = 0; k < n && ok; ++k) {
+            const int vi = ring + 2 * k + 1, ki = ring + 2 * k + 2;
+            if (!(ok = wait_kv(vi))) break;
+            for (int w = 0; w < 2 && ok; ++w) {
+              if (!(ok = wait_p(w))) break;
+              if (k == 0 && w == 0 && !(ok = wait_ofree())) break;
+              issue_pv(w, vi, k > 0);
+              pbits ^= 1u << w;
+              if (k == n - 1) tc_commit(O_FULL + 8 * w);
+              if (w == 1) tc_commit(KV_EMPTY + 8 * (vi % C::kStages));
+              if (k + 1 < n) {
+                if (w == 0 && !(ok = wait_kv(ki))) break;
+                issue_s(w, w, ki);
+                if (w == 1) {
+                  tc_commit(KV_EMPTY + 8 * (ki % C::kStages));
+                  if (k + 1 == n - 1) tc_commit(Q_EMPTY);
+                }
+              }
+            }
+          }
+        } else {
+          // ring order: K0, K1, then V_j followed by K_{j+2}
+          auto rK = [&](int k) { return ring + (k < 2 ? k : 2 * k - 1); };
+          auto rV = [&](int j) { return ring + (j <= n - 2 ? 2 + 2 * j : 2 * n - 1); };
+          if (!(ok = wait_kv(rK(0)))) break;
+          issue_s(0, 0, rK(0));
+          tc_commit(KV_EMPTY + 8 * (rK(0) % C::kStages));
+          if (n > 1) {
+            if (!(ok = wait_kv(rK(1)))) break;
+            issue_s(1, 0, rK(1));
+            tc_commit(KV_EMPTY + 8 * (rK(1) % C::kStages));
+          }
+          if (n <= 2) tc_commit(Q_EMPTY);
+          for (int j = 0; j < n && ok; ++j) {
+            const int w = j & 1;
+            if (!(ok = wait_kv(rV(j)))) break;
+            if (!(ok = wait_p(w))) break;
+            if (j == 0 && !(ok = wait_ofree())) break;
+            issue_pv(w, rV(j), j >= 2);
+            pbits ^= 1u << w;
+            tc_commit(KV_EMPTY + 8 * (rV(j) % C::kStages));
+            if (j + 2 >= n) tc_commit(O_FULL + 8 * w);
+            if (j + 2 < n) {
+              if (!(ok = wait_kv(rK(j + 2)))) break;
+              issue_s(w, 0, rK(j + 2));
+              tc_commit(KV_EMPTY + 8 * (rK(j + 2) % C::kStages));
+              if (j + 2 == n - 1) tc_commit(Q_EMPTY);
+            }
+          }
+        }
+        ring += 2 * n;
+        ++sg;
+      }
+      // drain: every MMA issued by this thread has completed before TMEM is freed
+      tc_commit(DRAIN);
+      drain_wait(DRAIN, 0);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax
+    const int w = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = w * 128, o_col = 256 + w * 128;
+    const float sl2 = a.scale_log2;
+    const int RG = pr.RG;
+    int cnt = 0, of0 = 0, of1 = 0, sg = 0;
+    bool ok = true;
+    long long t = t_begin;
+    Segment S;
+    while (ok && next_segment(pr, t, t_end, S)) {
+      const Loc& L = S.L;
+      const int n = S.n;
+      const int mt = (W == 2) ? w : 0;
+      const int node = (L.mp * W + mt) * npt + r / G;  // local node id of this row
+      const bool row_ok = r < npt * G && node < L.s.m;
+      const int prow = mt * npt * G + r;                 // row inside the row group
+      const int n_mine = (W == 2) ? n : (n - w + 1) / 2;
+      float m_run = -INFINITY, l_run = 0.f;
+      uint32_t anc[4] = {0u, 0u, 0u, 0u};
+      bool anc_ready = false;
+      for (int i = 0; i < n_mine; ++i) {
+        const int k = (W == 2) ? i : 2 * i + w;
+        const int tile = S.tile0 + k;
+        const bool is_tree = tile == L.tiles - 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(S_FULL + 8 * w, cnt & 1, abort_flag, kWaitNs));
+        if (!ok) break;
+        tc_fence_after();
+        if (is_tree && !anc_ready) {
+          anc_ready = true;
+          if (row_ok && !ancestor_bits(a.parent + L.s.n0, node, L.s.m, anc))
+            set_status(a.status, kStatusBadTree);
+        }
+        // keys of this tile: [0, lim) exist; the tree tile also needs the ancestor bit
+        const int lim = is_tree ? L.s.m : min(kKeyTile, L.s.P - tile * kKeyTile);
+        const bool full = !is_tree && lim == kKeyTile;
+        // pass 1: row maximum, 64 TMEM columns at a time
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t s[64];
+          tmem_ld32(tl + s_col + 64 * h, s);
+          tmem_ld32(tl + s_col + 64 * h + 32, s + 32);
+          tmem_wait_ld32(s);
+          tie32(s + 32);
+          if (!full) mask64(s, 64 * h, lim, is_tree, row_ok, anc);
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            mx0 = fmaxf(mx0, __uint_as_float(s[c]));
+            mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
+          }
+        }
+        const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
+        if (i == 0) {
+          m_run = m_new;
+        } else {
+          const bool need = m_new > m_run + 8.0f;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2(m_run - m_new) : 1.f;
+            if (need) {
+              l_run *= alpha;
+              m_run = m_new;
+            }
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t o[32];
+              tmem_ld32(tl + o_col + c0, o);
+              tmem_wait_ld32(o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tmem_st32(tl + o_col + c0, o);
+            }
+            tmem_wait_st();
+          }
+        }
+        const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
+        // pass 2: p = 2^(s * scale - m), packed as bf16 pairs into the already-read
+        // first half of the S buffer (P columns 32h.. come from S columns 64h..)
+        float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t s[64];
+          tmem_ld32(tl + s_col + 64 * h, s);
+          tmem_ld32(tl + s_col + 64 * h + 32, s + 32);
+          tmem_wait_ld32(s);
+          tie32(s + 32);
+          if (!full) mask64(s, 64 * h, lim, is_tree, row_ok, anc);
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, nb));
+            const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, nb));
+            ls0 += p0;
+            ls1 += p1;
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tl + s_col + 32 * h, pk);
+        }
+        l_run += ls0 + ls1;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(P_FULL + 8 * w);
+        ++cnt;
+      }
+      if (!ok) break;
+      // ---------------------------------------------------------------- epilogue
+      const size_t slot = (size_t)u + L.q;
+      float* orow = a.o_part + (slot * RG + prow) * D;
+      if (W == 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8 * w, (w == 0 ? of0 : of1) & 1, abort_flag, kWaitNs));
+        if (!ok) break;
+        (w == 0 ? of0 : of1)++;
+        tc_fence_after();
+        const float inv = 1.f / l_run;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tl + o_col + c0, o);
+          tmem_wait_ld32(o);
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(orow + c0 + e) =
+                  make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                              __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+          }
+        }
+        if (row_ok) a.lse_part[slot * RG + prow] = m_run + log2f(l_run);
+        tc_fence_before();
+        mbar_arrive(O_FREE);
+      } else if (w == 1) {
+        // Stream 1 may own no tile of this segment (or only one whose S was issued
+        // before the O_FREE wait), so nothing else keeps it from arriving for
+        // segment sg before segment sg-1's release completed: wait for that first.
+        if (sg > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(O_FREE, (sg - 1) & 1, abort_flag, kWaitNs));
+          if (!ok) break;
+        }
+        m1_s[(sg & 1) * 128 + r] = m_run;
+        l1_s[(sg & 1) * 128 + r] = l_run;
+        mbar_arrive(M1_READY);
+        mbar_arrive(O_FREE);
+      } else {
+        ok = __all_sync(0xffffffffu, mbar_wait(M1_READY, sg & 1, abort_flag, kWaitNs));
+        if (!ok) break;
+        const float m1 = m1_s[(sg & 1) * 128 + r];
+        const float l1 = l1_s[(sg & 1) * 128 + r];
+        const bool has1 = n > 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(O_FULL, of0 & 1, abort_flag, kWaitNs));
+        if (!ok) break;
+        ++of0;
+        if (has1) {
+          ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8, of1 & 1, abort_flag, kWaitNs));
+          if (!ok) break;
+          ++of1;
+        }
+        tc_fence_after();
+        const float mm = has1 ? fmaxf(m_run, m1) : m_run;
+        const float a0 = (m_run == -INFINITY) ? 0.f : ex2(m_run - mm);
+        const float a1 = (!has1 || m1 == -INFINITY) ? 0.f : ex2(m1 - mm);
+        const float lt = a0 * l_run + a1 * l1;
+        const float inv = 1.f / lt;
+        const float w0 = a0 * inv, w1 = a1 * inv;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t o[32], o1[32];
+          tmem_ld32(tl + 256 + c0, o);
+          tmem_ld32(tl + 384 + c0, o1);
+          tmem_wait_ld32(o);
+          tie32(o1);
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              float4 v;
+              v.x = __uint_as_float(o[e]) * w0 + (has1 ? __uint_as_float(o1[e]) * w1 : 0.f);
+              v.y = __uint_as_float(o[e + 1]) * w0 + (has1 ? __uint_as_float(o1[e + 1]) * w1 : 0.f);
+              v.z = __uint_as_float(o[e + 2]) * w0 + (has1 ? __uint_as_float(o1[e + 2]) * w1 : 0.f);
+              v.w = __uint_as_float(o[e + 3]) * w0 + (has1 ? __uint_as_float(o1[e + 3]) * w1 : 0.f);
+              *reinterpret_cast<float4*>(orow + c0 + e) = v;
+            }
+          }
+        }
+        if (row_ok) a.lse_part[slot * RG + prow] = mm + log2f(lt);
+        tc_fence_before();
+        mbar_arrive(O_FREE);
+      }
+      ++sg;
+    }
+  }
+  // ------------------------------------------------------------------ teardown
+  __syncwarp();
+  if (threadIdx.x == 0 && *abort_flag) set_status(a.status, kStatusTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) set_status(a.status, kStatusTimeout);
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// --------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D bf16 map over [rows][heads][d] with a box of {64, box_heads, box_rows}.
+bool make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows, int box_heads,
+              int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) {
+    record_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", 0, "entry point not found");
+    return false;
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    record_error("cuTensorMapEncodeTiled", (int)r, "tensor map rejected");
+    return false;
+  }
+  return true;
+}
+
+template <int D>
+cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s) {
+  const Problem& pr = a.pr;
+  CUtensorMap mq, mk, mv, mtk, mtv;
+  const void* kbase = pr.kv_capacity > 0 ? a.k_cache : a.tree_k;
+  const void* vbase = pr.kv_capacity > 0 ? a.v_cache : a.tree_v;
+  if (!make_map(&mq, a.q, D, pr.Hq, pr.node_capacity, pr.G, npt) ||
+      !make_map(&mk, kbase, D, pr.Hkv, pr.kv_capacity, 1, kKeyTile) ||
+      !make_map(&mv, vbase, D, pr.Hkv, pr.kv_capacity, 1, kKeyTile) ||
+      !make_map(&mtk, a.tree_k, D, pr.Hkv, pr.node_capacity, 1, kKeyTile) ||
+      !make_map(&mtv, a.tree_v, D, pr.Hkv, pr.node_capacity, 1, kKeyTile))
+    return cudaErrorInvalidValue;
+  constexpr int smem = Cfg<D>::kSmemBytes;
+  cudaError_t e = check_cuda(cudaFuncSetAttribute(partials_tc_kernel<D>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                             "cudaFuncSetAttribute(partials_tc_kernel)");
+  if (e != cudaSuccess) return e;
+  TcArgs ta{a, W, npt};
+  partials_tc_kernel<D><<<pr.U, kThreadsTc, smem, s>>>(mq, mk, mv, mtk, mtv, ta);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    cudaFuncAttributes fa{};
+    cudaFuncGetAttributes(&fa, partials_tc_kernel<D>);
+    char what[160];
+    snprintf(what, sizeof(what), "%s; kernel regs %d, max threads %d, smem %d+%d", cudaGetErrorString(e),
+             fa.numRegs, fa.maxThreadsPerBlock, (int)fa.sharedSizeBytes, smem);
+    record_error("launch partials_tc_kernel", (int)e, what);
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_partials_tc(const PartialArgs& a, int W, int npt, cudaStream_t s) {
+  return a.pr.d == 64 ? launch_tc_typed<64>(a, W, npt, s) : launch_tc_typed<128>(a, W, npt, s);
+}
+
+}  // namespace tva

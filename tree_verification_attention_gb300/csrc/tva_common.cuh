@@ -71,6 +71,17 @@ __device__ __forceinline__ SeqInfo seq_info(const Problem& pr, int b) {
   return s;
 }
 
+// Reports (once, from one thread) a cu_* entry outside the stated bounds.  The
+// offending sequence is treated as empty by every kernel.
+__device__ __forceinline__ void validate_sequences(const Problem& pr, int32_t* status) {
+  for (int b = 0; b < pr.B; ++b) {
+    if (!seq_info(pr, b).ok) {
+      set_status(status, kStatusInvalidArg);
+      return;
+    }
+  }
+}
+
 __device__ __forceinline__ int seq_tiles(int P) { return (P + kKeyTile - 1) / kKeyTile + 1; }
 __device__ __forceinline__ int seq_groups(const Problem& pr, int m) {
   return (m * pr.G + pr.RG - 1) / pr.RG;

@@ -2,11 +2,26 @@
 // kernel launches.  No torch types cross this boundary.
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
 #include "tva.h"
 #include "tva_internal.h"
+
+namespace {
+thread_local char g_last_error[256] = "";
+}  // namespace
+
+namespace tva {
+void record_error(const char* where, int code, const char* what) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, what, code);
+}
+cudaError_t check_cuda(cudaError_t e, const char* where) {
+  if (e != cudaSuccess) record_error(where, (int)e, cudaGetErrorString(e));
+  return e;
+}
+}  // namespace tva
 
 namespace {
 
@@ -16,11 +31,14 @@ constexpr int kMaxDevices = 64;
 
 int device_sms(int* sms) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  if (tva::check_cuda(cudaGetDevice(&dev), "cudaGetDevice") != cudaSuccess || dev < 0 ||
+      dev >= kMaxDevices)
+    return -1;
   static int cache[kMaxDevices] = {0};
   if (cache[dev] == 0) {
     int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    if (tva::check_cuda(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev),
+                        "cudaDeviceGetAttribute") != cudaSuccess || v <= 0)
       return -1;
     cache[dev] = v;
   }
@@ -34,6 +52,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 tva_status check_shape(int B, int Hq, int Hkv, int d, int dtype, int max_prefix, int max_nodes,
                        long long kv_cap, long long node_cap) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return TVA_ERR_INVALID_ARG;
+  if (Hq / Hkv > 128) return TVA_ERR_UNSUPPORTED;
   if (max_prefix < 0 || max_nodes < 1 || kv_cap < 0 || node_cap < 0) return TVA_ERR_INVALID_ARG;
   if (max_nodes > tva::kMaxNodes) return TVA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return TVA_ERR_UNSUPPORTED;
@@ -47,6 +66,7 @@ tva_status check_shape(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
 
 struct Layout {
   Problem pr;
+  int W, npt;
   size_t o_bytes, lse_bytes, total;
   long long slots;
 };
@@ -63,18 +83,23 @@ tva_status make_layout(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
   int sms = 0;
   if (device_sms(&sms) != 0) return TVA_ERR_CUDA;
   const int G = Hq / Hkv;
-  const int W = (max_nodes * G > 128) ? 2 : 1;
+  // Row groups hold whole nodes: an M-tile of 128 rows holds npt = floor(128 / G) nodes
+  // (all G query heads of a node), and a row group W <= 2 M-tiles.
+  const int npt = 128 / G;
+  const int W = (max_nodes > npt) ? 2 : 1;
+  L->npt = npt;
+  L->W = W;
   Problem& pr = L->pr;
   pr.cu_prefix = cu_prefix;
   pr.cu_nodes = cu_nodes;
   pr.single_prefix = single_prefix;
   pr.single_nodes = single_nodes;
   pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.G = G; pr.d = d;
-  pr.RG = 128 * W;
-  pr.U = sms * tva::simt_workers_per_sm();
+  pr.RG = W * npt * G;
+  pr.U = dtype == TVA_BF16 ? sms : sms * tva::simt_workers_per_sm();
   pr.max_prefix = max_prefix; pr.max_nodes = max_nodes;
   pr.kv_capacity = kv_cap; pr.node_capacity = node_cap;
-  const long long groups = (long long)B * Hkv * ((max_nodes * G + pr.RG - 1) / pr.RG);
+  const long long groups = (long long)B * Hkv * ((max_nodes + W * npt - 1) / (W * npt));
   L->slots = pr.U + groups;
   L->o_bytes = align256((size_t)L->slots * pr.RG * d * sizeof(float));
   L->lse_bytes = align256((size_t)L->slots * pr.RG * sizeof(float));
@@ -106,7 +131,9 @@ tva_status run_partials(const Layout& L, int dtype, float softmax_scale, const v
   a.o_part = static_cast<float*>(workspace);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.o_bytes);
   a.status = dev_status;
-  return tva::launch_partials_simt(a, dtype, s) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
+  const cudaError_t e = dtype == TVA_BF16 ? tva::launch_partials_tc(a, L.W, L.npt, s)
+                                          : tva::launch_partials_simt(a, dtype, s);
+  return e == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
 }
 
 tva_status run_combine(const Layout& L, int dtype, const void* workspace, void* out, float* lse,
@@ -148,6 +175,8 @@ OwnedState g_owned[kMaxDevices];
 }  // namespace
 
 extern "C" {
+
+const char* tva_last_error(void) { return g_last_error; }
 
 const char* tva_status_string(tva_status s) {
   switch (s) {

@@ -45,9 +45,16 @@ struct AcceptArgs {
   int32_t* status;
 };
 
+// Records a host-side failure for tva_last_error() (thread-local).
+void record_error(const char* where, int code, const char* what);
+// Records `e` (if it is an error) and returns it unchanged.
+cudaError_t check_cuda(cudaError_t e, const char* where);
+
 // dtype: 0 = bf16, 1 = fp32 (tva_dtype values)
 int simt_workers_per_sm();
 cudaError_t launch_partials_simt(const PartialArgs& a, int dtype, cudaStream_t s);
+// bf16, head_dim 64 or 128; W M-tiles of npt nodes per row group
+cudaError_t launch_partials_tc(const PartialArgs& a, int W, int npt, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 
