@@ -122,6 +122,25 @@ tva_status tree_verify_attn_combine(const tva_params* p, const void* workspace,
                                     size_t workspace_bytes, void* out, float* lse,
                                     int32_t* dev_status, void* stream);
 
+/* Same computation as tree_verify_attn_varlen, for callers that cannot allocate
+ * device memory (an engine that owns every allocation and forbids cudaMalloc on its
+ * execution path, or a plugin interface with no workspace argument).  The paper has no
+ * counterpart: this is a packaging of the same path.
+ * Scratch: a fixed 32 MiB array compiled into the library, reserved on every GPU that
+ * loads the library's device code and held until the process exits.  Problems whose
+ * tva_workspace_size() exceeds 32 MiB are rejected with TVA_ERR_WORKSPACE (see
+ * tva_last_error()) before anything is enqueued.  The first call on each device looks
+ * the array's device address up (cudaGetSymbolAddress), so make that first call
+ * before any stream capture.  Nothing here allocates.  All calls share the one array
+ * and its contents carry over between calls (no step needs it zeroed); calls whose
+ * work overlaps on the GPU (other streams, other host threads) race on it, so
+ * serialise them.  Arguments otherwise as for tree_verify_attn_varlen. */
+tva_status tree_verify_attn_varlen_noalloc(const tva_params* p, const void* q,
+                                           const void* k_cache, const void* v_cache,
+                                           const void* tree_k, const void* tree_v,
+                                           const int32_t* parent, void* out, float* lse,
+                                           int32_t* dev_status, void* stream);
+
 /* Single-sequence convenience form (B = 1).  prefix_len and num_nodes are host
  * values; every other pointer is a device pointer laid out as above with B = 1.
  * The workspace and the cu_* arrays are library-owned: allocated on first use per

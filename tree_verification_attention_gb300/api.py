@@ -247,3 +247,32 @@ def accept_longest_path(cu_nodes, parent, draft_tok, target_argmax, accept_len=N
         _ptr(accept_path), _ptr(next_token), _ptr(dev_status), _stream(stream))
     _check(code, "accept_longest_path")
     return accept_len, accept_path, next_token
+
+
+def tree_verify_attn_varlen_noalloc(q, k_cache, v_cache, tree_k, tree_v, parent, cu_prefix, cu_nodes,
+                                    max_prefix_len, max_nodes, out=None, lse=None, dev_status=None,
+                                    softmax_scale=0.0, stream=None, params=None):
+    """tree_verify_attn_varlen without a workspace argument, for callers that may not
+    allocate device memory: the library's fixed 32 MiB per-GPU scratch holds the
+    partials.  Larger problems raise TvaError (TVA_ERR_WORKSPACE).  Calls share that
+    scratch, so calls that overlap on the GPU must be serialised by the caller.
+    ``out``, ``lse`` and ``dev_status`` are allocated here only when not given."""
+    _attn_inputs(q, k_cache, v_cache, tree_k, tree_v, parent, cu_prefix, cu_nodes)
+    lib = load_library()
+    fn = lib.tree_verify_attn_varlen_noalloc
+    fn.restype = _I
+    fn.argtypes = [ctypes.POINTER(Params), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    p = params or make_params(q, k_cache, cu_prefix, cu_nodes, tree_k.shape[1], max_prefix_len,
+                              max_nodes, softmax_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    code = fn(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(tree_k), _ptr(tree_v),
+              _ptr(parent), _ptr(out), _ptr(lse), _ptr(dev_status), _stream(stream))
+    if code != 0:
+        detail = lib.tva_last_error().decode()
+        raise TvaError(code, "tree_verify_attn_varlen_noalloc" + (f" [{detail}]" if detail else ""))
+    return out, lse
