@@ -9,6 +9,7 @@
 // and a pointer 2^r levels up, so 7 rounds cover any depth <= 128.  A warp max over
 // the key (depth << 8 | 255 - i) picks the deepest accepted node, ties to the smaller
 // id; one lane then writes its root-first path.
+#include "tc_ptx.cuh"
 #include "tva_internal.h"
 
 namespace tva {
@@ -21,6 +22,9 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
   __shared__ int s_ok[kWarps][kMaxNodes];
   __shared__ int s_dep[kWarps][kMaxNodes];
   __shared__ int s_anc[kWarps][kMaxNodes];
+  __shared__ int s_slot[kWarps][kMaxNodes + 1];
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * kWarps + w;
   if (b >= a.B) return;  // whole warp leaves; no block-wide barrier follows
@@ -34,17 +38,29 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
     }
     return;
   }
+  // All of the sequence's inputs are fetched in one round of global loads: parents
+  // and draft tokens into registers, the m+1 target slots into shared memory.
   const int32_t* slot = a.target_argmax + n0 + b;
+  int par[kMaxNodes / 32], tok[kMaxNodes / 32];
+#pragma unroll
+  for (int k = 0; k < kMaxNodes / 32; ++k) {
+    const int i = lane + 32 * k;
+    par[k] = i < m ? __ldg(a.parent + n0 + i) : -1;
+    tok[k] = i < m ? __ldg(a.draft_tok + n0 + i) : 0;
+    if (i <= m) s_slot[w][i] = __ldg(slot + i);
+  }
+  if (lane == 0 && m == kMaxNodes) s_slot[w][kMaxNodes] = __ldg(slot + kMaxNodes);
+  __syncwarp();
   bool bad = false;
 #pragma unroll
   for (int k = 0; k < kMaxNodes / 32; ++k) {
     const int i = lane + 32 * k;
     if (i < m) {
-      const int p = __ldg(a.parent + n0 + i);
+      const int p = par[k];
       const bool pok = p >= -1 && p < i;
       bad |= !pok;
       s_par[w][i] = pok ? p : -1;
-      s_ok[w][i] = pok && __ldg(a.draft_tok + n0 + i) == __ldg(slot + p + 1);
+      s_ok[w][i] = pok && tok[k] == s_slot[w][p + 1];
       s_dep[w][i] = 1;
       s_anc[w][i] = pok ? p : -1;
     }
@@ -58,7 +74,7 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
     if (lane == 0) {
       set_status(a.status, kStatusBadTree);
       a.accept_len[b] = 0;
-      a.next_token[b] = __ldg(slot);
+      a.next_token[b] = s_slot[w][0];
     }
     return;
   }
@@ -113,7 +129,7 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
       j = s_par[w][j];
     }
     a.accept_len[b] = depth;
-    a.next_token[b] = __ldg(slot + best + 1);
+    a.next_token[b] = s_slot[w][best + 1];
   }
 }
 
@@ -121,8 +137,8 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
 
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s) {
   if (a.B <= 0) return cudaSuccess;
-  accept_kernel<<<(a.B + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(a);
-  return check_cuda(cudaGetLastError(), "launch accept_kernel");
+  return check_cuda(launch_pdl(accept_kernel, dim3((a.B + kWarps - 1) / kWarps), dim3(kWarps * 32), 0, s, a),
+                    "launch accept_kernel");
 }
 
 }  // namespace tva

@@ -11,15 +11,26 @@
 // exponentiating (the stable form of the same expression).
 //
 // One warp per (node, query head) row; each lane owns d/32 consecutive columns, so a
-// partial row is one coalesced 16-byte (d=128) or 8-byte (d=64) load per lane.
+// partial row is one coalesced 16-byte (d=128) or 8-byte (d=64) load per lane.  The
+// kernel is bound by the latency of those loads, so a warp issues up to 16 of them
+// before consuming any.  It is launched as a programmatic dependent of the partials
+// kernel: its blocks become resident early and wait for the partials to be complete.
+#include <type_traits>
+
+#include "tc_ptx.cuh"
 #include "tva_internal.h"
 
 namespace tva {
 namespace {
 
+constexpr int kBatch = 16;  // partial rows in flight per warp
+
 template <typename T, int D>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   constexpr int V = D / 32;
+  using Vec = typename std::conditional<V == 4, float4, float2>::type;
+  ptx::pdl_wait();  // partials (and every earlier write) are visible after this
+  ptx::pdl_launch_dependents();
   const Problem& pr = a.pr;
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -32,29 +43,54 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   const int u0 = (int)(R.start / c);
   const int u1 = (int)((R.start + R.tiles - 1) / c);
 
+  // Lane k (mod 32) holds the LSE of partial u0 + k: all of a row's LSE loads are in
+  // flight together, and the maximum / weights need only warp shuffles.
+  const int np = u1 - u0 + 1;
+  const float* lrow = a.lse_part + (size_t)(u0 + R.q) * pr.RG + R.r;
   float M = -INFINITY;
-  for (int u = u0; u <= u1; ++u)
-    M = fmaxf(M, __ldg(a.lse_part + (size_t)(u + R.q) * pr.RG + R.r));
+  for (int k = lane; k < np; k += 32) M = fmaxf(M, __ldg(lrow + (size_t)k * pr.RG));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
   float den = 0.f;
-  float acc[V];
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const float* obase = a.o_part + ((size_t)(u0 + R.q) * pr.RG + R.r) * D + lane * V;
+  const size_t ostride = (size_t)pr.RG * D;
+  for (int k0 = 0; k0 < np; k0 += 32) {
+    const int k = k0 + lane;
+    const float wk = k < np ? exp2f(__ldg(lrow + (size_t)k * pr.RG) - M) : 0.f;
+    den += wk;
+    for (int j0 = 0; j0 < 32 && k0 + j0 < np; j0 += kBatch) {
+      const int cnt = min(kBatch, np - k0 - j0);
+      float4 v[kBatch];
 #pragma unroll
-  for (int k = 0; k < V; ++k) acc[k] = 0.f;
-#pragma unroll 4
-  for (int u = u0; u <= u1; ++u) {
-    const size_t prow = (size_t)(u + R.q) * pr.RG + R.r;
-    const float w = exp2f(__ldg(a.lse_part + prow) - M);
-    den += w;
-    const float* op = a.o_part + prow * D + lane * V;
-    if constexpr (V == 4) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(op));
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-      acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
-    } else {
-      const float2 v = __ldg(reinterpret_cast<const float2*>(op));
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+      for (int j = 0; j < kBatch; ++j) {
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < cnt) {
+          const float* op = obase + (size_t)(k0 + j0 + j) * ostride;
+          if constexpr (V == 4) {
+            v[j] = __ldg(reinterpret_cast<const float4*>(op));
+          } else {
+            const float2 t = __ldg(reinterpret_cast<const float2*>(op));
+            v[j].x = t.x;
+            v[j].y = t.y;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, wk, j0 + j);
+        if (j < cnt) {
+          acc[0] = fmaf(wj, v[j].x, acc[0]);
+          acc[1] = fmaf(wj, v[j].y, acc[1]);
+          acc[2] = fmaf(wj, v[j].z, acc[2]);
+          acc[3] = fmaf(wj, v[j].w, acc[3]);
+        }
+      }
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   const float inv = 1.f / den;
   const size_t orow = ((size_t)n * pr.Hq + h) * D + lane * V;
   if constexpr (sizeof(T) == 4) {
@@ -75,8 +111,8 @@ cudaError_t launch_typed(const CombineArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.pr.node_capacity * a.pr.Hq;
   const long long blocks = (rows + 7) / 8;
   if (blocks <= 0) return cudaSuccess;
-  combine_kernel<T, D><<<(unsigned)blocks, 256, 0, s>>>(a);
-  return check_cuda(cudaGetLastError(), "launch combine_kernel");
+  return check_cuda(launch_pdl(combine_kernel<T, D>, dim3((unsigned)blocks), dim3(256), 0, s, a),
+                    "launch combine_kernel");
 }
 
 }  // namespace

@@ -118,6 +118,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
 
+  pdl_wait();  // launched as a programmatic dependent: inputs are final after this
+  pdl_launch_dependents();
   if (u == 0 && threadIdx.x == 0) validate_sequences(pr, a.status);
   const long long T_all = total_units(pr);
   const long long chunk = chunk_units(pr, T_all);
@@ -185,6 +187,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       long long t = t_begin;
       Segment S;
       const uint32_t q_box_bytes = 64u * G * npt * 2u;
+      const uint64_t evict_first = policy_evict_first();  // K/V are read once
       while (ok && next_segment(pr, t, t_end, S)) {
         const Loc& L = S.L;
         if (sg > 0 && !mbar_wait(Q_EMPTY, (sg - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
@@ -193,6 +196,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           for (int h = 0; h < C::kHalves; ++h)
             tma_load_3d(q_s + (mt * C::kHalves + h) * kHalfBytes, &tm_q, 64 * h, L.g * G,
                         L.s.n0 + (L.mp * W + mt) * npt, Q_FULL);
+        const int n = S.n;
         auto load = [&](int k, bool is_v) -> bool {
           const int stage = ring % C::kStages, use = ring / C::kStages;
           if (use > 0 && !mbar_wait(KV_EMPTY + 8 * stage, (use - 1) & 1, abort_flag, kWaitNs))
@@ -203,12 +207,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const int z = tree ? L.s.n0 : L.s.p0 + tile * kKeyTile;
           mbar_expect_tx(KV_FULL + 8 * stage, C::kTileBytes);
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(kv_s + stage * C::kTileBytes + h * kHalfBytes, m, 64 * h, L.g, z,
-                        KV_FULL + 8 * stage);
+            tma_load_3d_hint(kv_s + stage * C::kTileBytes + h * kHalfBytes, m, 64 * h, L.g, z,
+                             KV_FULL + 8 * stage, evict_first);
           ++ring;
           return true;
         };
-        const int n = S.n;
         if (W == 2) {
           for (int k = 0; k < n && ok; ++k) ok = load(k, false) && load(k, true);
         } else {
@@ -596,8 +599,8 @@ cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s
                              "cudaFuncSetAttribute(partials_tc_kernel)");
   if (e != cudaSuccess) return e;
   TcArgs ta{a, W, npt};
-  partials_tc_kernel<D><<<pr.U, kThreadsTc, smem, s>>>(mq, mk, mv, mtk, mtv, ta);
-  e = cudaGetLastError();
+  e = launch_pdl(partials_tc_kernel<D>, dim3(pr.U), dim3(kThreadsTc), (size_t)smem, s, mq, mk, mv, mtk,
+                 mtv, ta);
   if (e != cudaSuccess) {
     cudaFuncAttributes fa{};
     cudaFuncGetAttributes(&fa, partials_tc_kernel<D>);

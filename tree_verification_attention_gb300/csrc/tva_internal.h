@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "tva_common.cuh"
@@ -49,6 +50,25 @@ struct AcceptArgs {
 void record_error(const char* where, int code, const char* what);
 // Records `e` (if it is an error) and returns it unchanged.
 cudaError_t check_cuda(cudaError_t e, const char* where);
+
+// Launches `kernel` allowing programmatic dependent launch: the kernel may become
+// resident while the previous kernel in the stream still runs, and must call
+// griddepcontrol.wait (ptx::pdl_wait) before touching memory that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // dtype: 0 = bf16, 1 = fp32 (tva_dtype values)
 int simt_workers_per_sm();
