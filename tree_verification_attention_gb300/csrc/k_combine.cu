@@ -24,6 +24,7 @@ namespace tva {
 namespace {
 
 constexpr int kBatch = 16;  // partial rows in flight per warp
+constexpr int kCuCap = 2048;  // ints of shared memory for the staged cu_* arrays
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
@@ -31,7 +32,9 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   using Vec = typename std::conditional<V == 4, float4, float2>::type;
   ptx::pdl_wait();  // partials (and every earlier write) are visible after this
   ptx::pdl_launch_dependents();
-  const Problem& pr = a.pr;
+  __shared__ int cu_buf[kCuCap];
+  Problem pr = a.pr;
+  stage_cu(pr, cu_buf, kCuCap);
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= (long long)pr.node_capacity * pr.Hq) return;
@@ -43,39 +46,47 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   const int u0 = (int)(R.start / c);
   const int u1 = (int)((R.start + R.tiles - 1) / c);
 
-  // Lane k (mod 32) holds the LSE of partial u0 + k: all of a row's LSE loads are in
-  // flight together, and the maximum / weights need only warp shuffles.
+  // Lane k (mod 32) holds the LSE of partial u0 + k.  The first kBatch partial rows
+  // of O are requested together with the LSEs (they do not depend on the maximum), so
+  // a row with up to kBatch partials costs one round of loads.
   const int np = u1 - u0 + 1;
+  if ((long long)u1 + R.q >= a.slots) {  // cannot happen for a consistent layout
+    if (lane == 0) set_status(a.status, kStatusInvalidArg);
+    return;
+  }
   const float* lrow = a.lse_part + (size_t)(u0 + R.q) * pr.RG + R.r;
-  float M = -INFINITY;
-  for (int k = lane; k < np; k += 32) M = fmaxf(M, __ldg(lrow + (size_t)k * pr.RG));
+  const float* obase = a.o_part + ((size_t)(u0 + R.q) * pr.RG + R.r) * D + lane * V;
+  const size_t ostride = (size_t)pr.RG * D;
+  auto load_o = [&](int k) -> float4 {
+    const float* op = obase + (size_t)k * ostride;
+    if constexpr (V == 4) {
+      return __ldg(reinterpret_cast<const float4*>(op));
+    } else {
+      const float2 t = __ldg(reinterpret_cast<const float2*>(op));
+      return make_float4(t.x, t.y, 0.f, 0.f);
+    }
+  };
+  float lk = lane < np ? __ldg(lrow + (size_t)lane * pr.RG) : -INFINITY;
+  float4 v[kBatch];
+  const int cnt0 = min(kBatch, np);
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j) v[j] = j < cnt0 ? load_o(j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float M = lk;
+  for (int k = lane + 32; k < np; k += 32) M = fmaxf(M, __ldg(lrow + (size_t)k * pr.RG));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
 
   float den = 0.f;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const float* obase = a.o_part + ((size_t)(u0 + R.q) * pr.RG + R.r) * D + lane * V;
-  const size_t ostride = (size_t)pr.RG * D;
   for (int k0 = 0; k0 < np; k0 += 32) {
-    const int k = k0 + lane;
-    const float wk = k < np ? exp2f(__ldg(lrow + (size_t)k * pr.RG) - M) : 0.f;
+    if (k0 > 0) lk = k0 + lane < np ? __ldg(lrow + (size_t)(k0 + lane) * pr.RG) : -INFINITY;
+    const float wk = k0 + lane < np ? exp2f(lk - M) : 0.f;
     den += wk;
     for (int j0 = 0; j0 < 32 && k0 + j0 < np; j0 += kBatch) {
       const int cnt = min(kBatch, np - k0 - j0);
-      float4 v[kBatch];
+      if (k0 + j0 > 0) {
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < cnt) {
-          const float* op = obase + (size_t)(k0 + j0 + j) * ostride;
-          if constexpr (V == 4) {
-            v[j] = __ldg(reinterpret_cast<const float4*>(op));
-          } else {
-            const float2 t = __ldg(reinterpret_cast<const float2*>(op));
-            v[j].x = t.x;
-            v[j].y = t.y;
-          }
-        }
+        for (int j = 0; j < kBatch; ++j) v[j] = j < cnt ? load_o(k0 + j0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {

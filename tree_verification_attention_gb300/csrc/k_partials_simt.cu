@@ -42,7 +42,9 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
   uint32_t* masks = reinterpret_cast<uint32_t*>(ps + kRB * (kKT + 1));  // [128][4]
   __shared__ int tree_bad;
 
-  const Problem& pr = a.pr;
+  __shared__ int cu_buf[512];
+  Problem pr = a.pr;
+  stage_cu(pr, cu_buf, 512);
   const T* __restrict__ q = static_cast<const T*>(a.q);
   const int tid = threadIdx.x;
   const int r_loc = tid >> 3;  // row of this thread inside the block
@@ -63,6 +65,8 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
     const bool has_tree = tile1 == L.tiles;
     const SeqInfo s = L.s;
     const int slot = u + L.q;
+    const bool slot_ok = slot < a.slots;  // cannot fail for a consistent layout
+    if (!slot_ok && tid == 0) set_status(a.status, kStatusInvalidArg);
 
     if (has_tree) {
       __syncthreads();
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
           }
         }
       }
-      if (row_ok) {
+      if (row_ok && slot_ok) {
         const float inv = 1.f / l_run;
         float* op = a.o_part + ((size_t)slot * pr.RG + (my_row - row_begin)) * D;
 #pragma unroll

@@ -56,7 +56,9 @@ struct Cfg {
   static constexpr int kStages = D == 128 ? 4 : 8;
   static constexpr int kQBytes = 2 * kHalves * kHalfBytes;
   static constexpr int kBarOff = kQBytes + kStages * kTileBytes;
-  static constexpr int kMiscBytes = 4096;
+  static constexpr int kCuOff = 4096;               // staged cu_* arrays inside misc
+  static constexpr int kCuCap = 1024;               // ints: batches up to 511 sequences
+  static constexpr int kMiscBytes = kCuOff + 4 * kCuCap;
   static constexpr int kSmemBytes = kBarOff + kMiscBytes + 1024;  // + alignment slack
 };
 
@@ -82,17 +84,24 @@ __device__ __forceinline__ bool next_segment(const Problem& pr, long long& t, lo
   return true;
 }
 
-// Logits of keys c0 .. c0+63 that the row does not see become -inf: keys at or past
-// `lim`, and in the tree tile keys that are not the row's node or its ancestors.
-__device__ __forceinline__ void mask64(uint32_t* s, int c0, int lim, bool is_tree, bool row_ok,
-                                       const uint32_t* anc) {
-#pragma unroll
-  for (int e = 0; e < 64; ++e) {
-    const int c = c0 + e;
-    bool vis = c < lim;
-    if (is_tree) vis = vis && row_ok && ((anc[c >> 5] >> (c & 31)) & 1u);
-    if (!vis) s[e] = kNegInfBits;
+// Ancestor-or-self bits of node i from the sequence's parent ids in shared memory.
+// False (only i's own bit set) when a parent met on the walk is outside [-1, node).
+__device__ __forceinline__ bool ancestor_bits_shared(const int* par, int i, uint32_t bits[4]) {
+  bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+  bits[i >> 5] |= 1u << (i & 31);
+  int j = i;
+  for (int steps = 0; steps < kMaxNodes; ++steps) {
+    const int p = par[j];
+    if (p < -1 || p >= j) {
+      bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+      bits[i >> 5] |= 1u << (i & 31);
+      return false;
+    }
+    if (p < 0) return true;
+    bits[p >> 5] |= 1u << (p & 31);
+    j = p;
   }
+  return true;
 }
 
 // Waits that ignore the abort flag (used only while draining).
@@ -113,13 +122,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const PartialArgs& a = args.a;
-  const Problem& pr = a.pr;
-  const int W = args.W, npt = args.npt, G = pr.G;
+  Problem* pr_s = reinterpret_cast<Problem*>(smem + C::kBarOff + C::kCuOff - 128);
+  const Problem& pr = *pr_s;
+  const int W = args.W, npt = args.npt, G = a.pr.G;  // kernel parameters: readable before staging
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
 
   pdl_wait();  // launched as a programmatic dependent: inputs are final after this
   pdl_launch_dependents();
+  stage_problem(a.pr, pr_s, reinterpret_cast<int*>(smem + C::kBarOff + C::kCuOff), C::kCuCap);
   if (u == 0 && threadIdx.x == 0) validate_sequences(pr, a.status);
   const long long T_all = total_units(pr);
   const long long chunk = chunk_units(pr, T_all);
@@ -141,7 +152,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t O_FREE = O_FULL + 16;
   const uint32_t M1_READY = O_FREE + 8;
   const uint32_t DRAIN = M1_READY + 8;
-  uint8_t* misc = smem + C::kBarOff + 16 * C::kStages + 8 * 12;
+  const uint32_t PAR_READY = DRAIN + 8;                 // [2]
+  uint8_t* misc = smem + C::kBarOff + 16 * C::kStages + 8 * 14;
+  int* par_s = reinterpret_cast<int*>(smem + C::kBarOff + 2560);   // [2][128] parent ids
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   float* m1_s = reinterpret_cast<float*>(smem + C::kBarOff + 512);  // [2][128]
@@ -162,6 +175,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(O_FREE, 256);
     mbar_init(M1_READY, 128);
     mbar_init(DRAIN, 1);
+    mbar_init(PAR_READY, 128);
+    mbar_init(PAR_READY + 8, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -350,21 +365,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const uint32_t s_col = w * 128, o_col = 256 + w * 128;
     const float sl2 = a.scale_log2;
     const int RG = pr.RG;
-    int cnt = 0, of0 = 0, of1 = 0, sg = 0;
+    int cnt = 0, of0 = 0, of1 = 0, sg = 0, trees = 0;
     bool ok = true;
     long long t = t_begin;
     Segment S;
     while (ok && next_segment(pr, t, t_end, S)) {
       const Loc& L = S.L;
       const int n = S.n;
+      // The tree tile needs every parent id of the sequence.  Issue those loads now
+      // (one per thread) so their latency hides behind the prefix tiles; they are
+      // shared through shared memory when the tree tile comes.
+      const int my_parent = (S.tile0 + n == L.tiles && r < L.s.m) ? __ldg(a.parent + L.s.n0 + r) : 0;
       const int mt = (W == 2) ? w : 0;
       const int node = (L.mp * W + mt) * npt + r / G;  // local node id of this row
-      const bool row_ok = r < npt * G && node < L.s.m;
+      bool row_ok = r < npt * G && node < L.s.m;
       const int prow = mt * npt * G + r;                 // row inside the row group
       const int n_mine = (W == 2) ? n : (n - w + 1) / 2;
       float m_run = -INFINITY, l_run = 0.f;
-      uint32_t anc[4] = {0u, 0u, 0u, 0u};
-      bool anc_ready = false;
       for (int i = 0; i < n_mine; ++i) {
         const int k = (W == 2) ? i : 2 * i + w;
         const int tile = S.tile0 + k;
@@ -372,14 +389,41 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(S_FULL + 8 * w, cnt & 1, abort_flag, kWaitNs));
         if (!ok) break;
         tc_fence_after();
-        if (is_tree && !anc_ready) {
-          anc_ready = true;
-          if (row_ok && !ancestor_bits(a.parent + L.s.n0, node, L.s.m, anc))
-            set_status(a.status, kStatusBadTree);
-        }
         // keys of this tile: [0, lim) exist; the tree tile also needs the ancestor bit
         const int lim = is_tree ? L.s.m : min(kKeyTile, L.s.P - tile * kKeyTile);
-        const bool full = !is_tree && lim == kKeyTile;
+        if (is_tree || lim < kKeyTile) {
+          // Rare tiles (the last, partial prefix tile; the tree tile): rewrite the logits
+          // the row does not see to -inf in TMEM, 32 columns at a time, so the two
+          // passes below carry no masking code.
+          uint32_t anc[4] = {0u, 0u, 0u, 0u};
+          if (is_tree) {
+            // the segment's parent ids, loaded at its start, meet in shared memory
+            int* ps = par_s + w * 128;
+            if (r < L.s.m) ps[r] = my_parent;
+            mbar_arrive(PAR_READY + 8 * w);
+            ok = __all_sync(0xffffffffu, mbar_wait(PAR_READY + 8 * w, trees & 1, abort_flag, kWaitNs));
+            ++trees;
+            if (!ok) break;
+            if (row_ok && !ancestor_bits_shared(ps, node, anc)) set_status(a.status, kStatusBadTree);
+          }
+#pragma unroll 1
+          for (int ck = 0; ck < 4; ++ck) {
+            uint32_t sv[32];
+            tmem_ld32(tl + s_col + 32 * ck, sv);
+            tmem_wait_ld32(sv);
+            const int rem = lim - 32 * ck;
+            uint32_t vw = rem >= 32 ? 0xffffffffu : (rem <= 0 ? 0u : (1u << rem) - 1u);
+            if (is_tree) {
+              const uint32_t aw = ck == 0 ? anc[0] : ck == 1 ? anc[1] : ck == 2 ? anc[2] : anc[3];
+              vw &= row_ok ? aw : 0u;
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!((vw >> e) & 1u)) sv[e] = kNegInfBits;
+            tmem_st32(tl + s_col + 32 * ck, sv);
+          }
+          tmem_wait_st();
+        }
         // pass 1: row maximum, 64 TMEM columns at a time
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -389,7 +433,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tmem_ld32(tl + s_col + 64 * h + 32, s + 32);
           tmem_wait_ld32(s);
           tie32(s + 32);
-          if (!full) mask64(s, 64 * h, lim, is_tree, row_ok, anc);
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
             mx0 = fmaxf(mx0, __uint_as_float(s[c]));
@@ -430,7 +473,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tmem_ld32(tl + s_col + 64 * h + 32, s + 32);
           tmem_wait_ld32(s);
           tie32(s + 32);
-          if (!full) mask64(s, 64 * h, lim, is_tree, row_ok, anc);
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
@@ -451,6 +493,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
       const size_t slot = (size_t)u + L.q;
+      if (slot >= (size_t)a.slots) {  // cannot happen for a consistent layout; never write past it
+        set_status(a.status, kStatusInvalidArg);
+        row_ok = false;
+      }
       float* orow = a.o_part + (slot * RG + prow) * D;
       if (W == 2) {
         ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8 * w, (w == 0 ? of0 : of1) & 1, abort_flag, kWaitNs));

@@ -60,15 +60,55 @@ __device__ __forceinline__ SeqInfo seq_info(const Problem& pr, int b) {
   if (pr.cu_prefix == nullptr) {
     s.p0 = 0; s.P = pr.single_prefix; s.n0 = 0; s.m = pr.single_nodes;
   } else {
-    s.p0 = __ldg(pr.cu_prefix + b);
-    s.P = __ldg(pr.cu_prefix + b + 1) - s.p0;
-    s.n0 = __ldg(pr.cu_nodes + b);
-    s.m = __ldg(pr.cu_nodes + b + 1) - s.n0;
+    // plain (generic) loads: the arrays may have been staged in shared memory
+    s.p0 = pr.cu_prefix[b];
+    s.P = pr.cu_prefix[b + 1] - s.p0;
+    s.n0 = pr.cu_nodes[b];
+    s.m = pr.cu_nodes[b + 1] - s.n0;
   }
   s.ok = s.p0 >= 0 && s.P >= 0 && s.P <= pr.max_prefix && s.p0 + s.P <= pr.kv_capacity &&
          s.n0 >= 0 && s.m >= 0 && s.m <= pr.max_nodes && s.n0 + s.m <= pr.node_capacity;
   if (!s.ok) { s.P = 0; s.m = 0; }
   return s;
+}
+
+// Copies cu_prefix / cu_nodes into `buf` (2 * (B + 1) ints of shared memory) when they
+// fit in `cap` ints, and points `pr` at the copies, so that the sequence walks below
+// cost shared-memory loads instead of one round of global loads per sequence.  Every
+// thread of the block must call it; it ends with a block barrier.
+__device__ __forceinline__ void stage_cu(Problem& pr, int* buf, int cap) {
+  const bool fits = pr.cu_prefix != nullptr && 2 * (pr.B + 1) <= cap;
+  if (fits) {
+    for (int i = threadIdx.x; i <= pr.B; i += blockDim.x) {
+      buf[i] = __ldg(pr.cu_prefix + i);
+      buf[pr.B + 1 + i] = __ldg(pr.cu_nodes + i);
+    }
+  }
+  __syncthreads();
+  if (fits) {
+    pr.cu_prefix = buf;
+    pr.cu_nodes = buf + pr.B + 1;
+  }
+}
+
+// Same, but the resulting problem description is also placed in shared memory (`dst`),
+// so that kernels short of registers can read its fields from there.
+__device__ __forceinline__ void stage_problem(const Problem& src, Problem* dst, int* buf, int cap) {
+  const bool fits = src.cu_prefix != nullptr && 2 * (src.B + 1) <= cap;
+  if (fits) {
+    for (int i = threadIdx.x; i <= src.B; i += blockDim.x) {
+      buf[i] = __ldg(src.cu_prefix + i);
+      buf[src.B + 1 + i] = __ldg(src.cu_nodes + i);
+    }
+  }
+  if (threadIdx.x == 0) {
+    *dst = src;
+    if (fits) {
+      dst->cu_prefix = buf;
+      dst->cu_nodes = buf + src.B + 1;
+    }
+  }
+  __syncthreads();
 }
 
 // Reports (once, from one thread) a cu_* entry outside the stated bounds.  The

@@ -130,6 +130,7 @@ tva_status run_partials(const Layout& L, int dtype, float softmax_scale, const v
   a.scale_log2 = scale_log2(softmax_scale, L.pr.d);
   a.o_part = static_cast<float*>(workspace);
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.o_bytes);
+  a.slots = L.slots;
   a.status = dev_status;
   const cudaError_t e = dtype == TVA_BF16 ? tva::launch_partials_tc(a, L.W, L.npt, s)
                                           : tva::launch_partials_simt(a, dtype, s);
@@ -142,6 +143,7 @@ tva_status run_combine(const Layout& L, int dtype, const void* workspace, void* 
   a.pr = L.pr;
   a.o_part = static_cast<const float*>(workspace);
   a.lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + L.o_bytes);
+  a.slots = L.slots;
   a.out = out; a.lse = lse; a.status = dev_status;
   return tva::launch_combine(a, dtype, s) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
 }

@@ -21,6 +21,7 @@ struct PartialArgs {
   float scale_log2;   // softmax_scale * log2(e): logits are kept in base 2
   float* o_part;      // [slots][RG][d] normalised partial outputs
   float* lse_part;    // [slots][RG] partial log2-sum-exp2 of the base-2 logits
+  long long slots;    // slots the workspace holds (writes beyond are refused)
   int32_t* status;
 };
 
@@ -28,6 +29,7 @@ struct CombineArgs {
   Problem pr;
   const float* o_part;
   const float* lse_part;
+  long long slots;
   void* out;
   float* lse;
   int32_t* status;
