@@ -260,23 +260,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_after();
         return true;
       };
+      // Operand descriptors: built once, then stepped through their low word (the issue
+      // rate of this one thread bounds the tensor pipe, so each MMA costs as few
+      // instructions as possible).  K / Q are K-major, V is MN-major (d contiguous).
+      const uint32_t k_hi = (uint32_t)(sdesc_sw128(0, 16, 1024) >> 32);
+      const uint32_t v_hi = (uint32_t)(sdesc_sw128(0, kHalfBytes, 1024) >> 32);
+      const uint32_t k_lo = (uint32_t)sdesc_sw128(kv_s, 16, 1024);
+      const uint32_t v_lo = (uint32_t)sdesc_sw128(kv_s, kHalfBytes, 1024);
+      const uint32_t q_lo = (uint32_t)sdesc_sw128(q_s, 16, 1024);
       auto issue_s = [&](int w, int mt, int idx) {
-        const uint32_t kb = kv_s + (idx % C::kStages) * C::kTileBytes;
-        const uint32_t qb = q_s + mt * C::kHalves * kHalfBytes;
+        const uint32_t kl = k_lo + (uint32_t)((idx % C::kStages) * C::kTileBytes >> 4);
+        const uint32_t ql = q_lo + (uint32_t)(mt * C::kHalves * kHalfBytes >> 4);
+        const uint32_t dt = tmem + w * 128;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-          mma_ss(tmem + w * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                 idesc_s, ks > 0);
+          const uint32_t o = (uint32_t)((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+          mma_ss(dt, desc_join(ql + o, k_hi), desc_join(kl + o, k_hi), idesc_s, ks > 0);
         }
         tc_commit(S_FULL + 8 * w);
       };
       auto issue_pv = [&](int w, int idx, bool acc) {
-        const uint32_t vb = kv_s + (idx % C::kStages) * C::kTileBytes;
+        const uint32_t vl = v_lo + (uint32_t)((idx % C::kStages) * C::kTileBytes >> 4);
+        const uint32_t dt = tmem + 256 + w * 128, at = tmem + w * 128;
 #pragma unroll
         for (int ks = 0; ks < kKeyTile / 16; ++ks)
-          mma_ts(tmem + 256 + w * 128, tmem + w * 128 + ks * 8,
-                 sdesc_sw128(vb + ks * 2048, kHalfBytes, 1024), idesc_o, (acc || ks > 0) ? 1u : 0u);
+          mma_ts(dt, at + ks * 8, desc_join(vl + (uint32_t)(ks * 2048 >> 4), v_hi), idesc_o,
+                 (acc || ks > 0) ? 1u : 0u);
       };
       auto wait_p = [&](int w) -> bool {
         if (!mbar_wait(P_FULL + 8 * w, (pbits >> w) & 1u, abort_flag, kWaitNs)) return false;
