@@ -443,9 +443,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           tmem_wait_ld32(s);
           tie32(s + 32);
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            mx0 = fmaxf(mx0, __uint_as_float(s[c]));
-            mx1 = fmaxf(mx1, __uint_as_float(s[c + 1]));
+          for (int c = 0; c < 64; c += 4) {
+            mx0 = max3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+            mx1 = max3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
           }
         }
         const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
@@ -473,8 +473,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
         // pass 2: p = 2^(s * scale - m), packed as bf16 pairs into the already-read
-        // first half of the S buffer (P columns 32h.. come from S columns 64h..)
-        float ls0 = 0.f, ls1 = 0.f;
+        // first half of the S buffer (P columns 32h.. come from S columns 64h..).
+        // The scaling and the row sum run on packed fp32 pairs.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nbx2 = f2_pack(nb, nb);
+        uint64_t lsx2 = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t s[64];
@@ -485,14 +487,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, nb));
-            const float p1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, nb));
-            ls0 += p0;
-            ls1 += p1;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2x2, nbx2),
+                      x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            lsx2 = f2_add(lsx2, f2_pack(p0, p1));
             pk[c] = pack_bf16x2(p0, p1);
           }
           tmem_st32(tl + s_col + 32 * h, pk);
         }
+        float ls0, ls1;
+        f2_unpack(lsx2, ls0, ls1);
         l_run += ls0 + ls1;
         tmem_wait_st();
         tc_fence_before();
