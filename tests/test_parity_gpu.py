@@ -45,6 +45,9 @@ EDGE = [
     dict(batch=2, Hq=6, Hkv=3, d=128, prefix=129, m=40, tree="chain", dtype="fp32", vocab=8),
     dict(batch=2, Hq=2, Hkv=1, d=64, prefix=(0, 0), m=5, tree="random", dtype="fp32", vocab=8),
     dict(batch=5, Hq=32, Hkv=8, d=128, prefix=(1, 600), m=1, tree="chain", dtype="bf16", vocab=8),
+    # GQA groups that do not divide 128: M-tiles of 126 / 125 rows, padded in the partials
+    dict(batch=2, Hq=12, Hkv=4, d=128, prefix=(77, 200), m=50, tree="random", dtype="bf16", vocab=8),
+    dict(batch=1, Hq=10, Hkv=2, d=64, prefix=300, m=30, tree="random", dtype="fp32", vocab=8),
 ]
 
 

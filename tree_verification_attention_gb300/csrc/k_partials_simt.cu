@@ -168,10 +168,15 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
       }
       if (row_ok && slot_ok) {
         const float inv = 1.f / l_run;
-        float* op = a.o_part + ((size_t)slot * pr.RG + (my_row - row_begin)) * D;
+        const int rr = my_row - row_begin, MT = mtile_rows(pr.G);
+        const int pp = rr / MT * 128 + rr % MT;  // padded row (see o_part_offset)
+        const int RGP = padded_group_rows(pr.RG, pr.G);
 #pragma unroll
-        for (int k = 0; k < D / 8; ++k) op[kg + 8 * k] = o[k] * inv;
-        if (kg == 0) a.lse_part[(size_t)slot * pr.RG + (my_row - row_begin)] = m_run + log2f(l_run);
+        for (int k = 0; k < D / 8; ++k) {
+          const int c = kg + 8 * k;
+          a.o_part[o_part_offset(slot, pp, c >> 2, RGP, D) + (c & 3)] = o[k] * inv;
+        }
+        if (kg == 0) a.lse_part[(size_t)slot * RGP + pp] = m_run + log2f(l_run);
       }
     }
     t = seg_end;

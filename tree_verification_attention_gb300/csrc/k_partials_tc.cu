@@ -388,7 +388,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int mt = (W == 2) ? w : 0;
       const int node = (L.mp * W + mt) * npt + r / G;  // local node id of this row
       bool row_ok = r < npt * G && node < L.s.m;
-      const int prow = mt * npt * G + r;                 // row inside the row group
       const int n_mine = (W == 2) ? n : (n - w + 1) / 2;
       float m_run = -INFINITY, l_run = 0.f;
       for (int i = 0; i < n_mine; ++i) {
@@ -511,7 +510,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         set_status(a.status, kStatusInvalidArg);
         row_ok = false;
       }
-      float* orow = a.o_part + (slot * RG + prow) * D;
+      const int pp = mt * 128 + r;  // padded row: lane = row within a 32-row block
+      float* oblk = a.o_part + o_part_offset(slot, pp, 0, W * 128, D);
       if (W == 2) {
         ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8 * w, (w == 0 ? of0 : of1) & 1, abort_flag, kWaitNs));
         if (!ok) break;
@@ -526,12 +526,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           if (row_ok) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(orow + c0 + e) =
+              *reinterpret_cast<float4*>(oblk + (c0 + e) * 32) =
                   make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                               __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
           }
         }
-        if (row_ok) a.lse_part[slot * RG + prow] = m_run + log2f(l_run);
+        if (row_ok) a.lse_part[slot * (W * 128) + pp] = m_run + log2f(l_run);
         tc_fence_before();
         mbar_arrive(O_FREE);
       } else if (w == 1) {
@@ -582,11 +582,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
               v.y = __uint_as_float(o[e + 1]) * w0 + (has1 ? __uint_as_float(o1[e + 1]) * w1 : 0.f);
               v.z = __uint_as_float(o[e + 2]) * w0 + (has1 ? __uint_as_float(o1[e + 2]) * w1 : 0.f);
               v.w = __uint_as_float(o[e + 3]) * w0 + (has1 ? __uint_as_float(o1[e + 3]) * w1 : 0.f);
-              *reinterpret_cast<float4*>(orow + c0 + e) = v;
+              *reinterpret_cast<float4*>(oblk + (c0 + e) * 32) = v;
             }
           }
         }
-        if (row_ok) a.lse_part[slot * RG + prow] = mm + log2f(lt);
+        if (row_ok) a.lse_part[slot * (W * 128) + pp] = mm + log2f(lt);
         tc_fence_before();
         mbar_arrive(O_FREE);
       }

@@ -212,6 +212,53 @@ __device__ __forceinline__ bool locate_row(const Problem& pr, int n, int h, RowL
   return found;
 }
 
+// Partial-output layout.  A row group of RG = W * MT rows (W M-tiles of MT =
+// floor(128 / G) * G rows) occupies W * 128 padded rows per slot: row r of M-tile mt is
+// padded row mt * 128 + r.  LSE partials are [slot][padded row].  O partials are stored
+// in 32-row blocks, each column-group major - [block][d / 4][32 rows][4 floats] - so that
+// a warp whose lanes hold 32 consecutive rows writes, and the combine reads, 512
+// contiguous bytes per 16-byte access.
+__host__ __device__ __forceinline__ int mtile_rows(int G) { return (128 / G) * G; }
+__host__ __device__ __forceinline__ int padded_group_rows(int RG, int G) { return RG / mtile_rows(G) * 128; }
+// float offset of column group cg (4 floats) of padded row pp in slot `slot`
+__host__ __device__ __forceinline__ size_t o_part_offset(size_t slot, int pp, int cg, int RGP, int D) {
+  return (slot * RGP + (pp & ~31)) * D + (size_t)cg * 128 + (pp & 31) * 4;
+}
+
+// Where row group qg lives, for the combine.
+struct GroupLoc {
+  SeqInfo s;
+  int b, g, mp;       // sequence, KV head, row group within (b, g)
+  int tiles;          // units of the row group
+  long long start;    // first unit of the row group
+  long long T;        // total units
+  bool found;
+};
+
+__device__ __forceinline__ GroupLoc locate_group(const Problem& pr, long long qg) {
+  GroupLoc R;
+  R.found = false;
+  R.b = R.g = R.mp = R.tiles = 0;
+  R.start = 0;
+  long long acc = 0, qacc = 0;
+  for (int b = 0; b < pr.B; ++b) {
+    const SeqInfo s = seq_info(pr, b);
+    const int MP = seq_groups(pr, s.m);
+    const int tiles = seq_tiles(s.P);
+    const long long nq = (long long)pr.Hkv * MP;
+    if (!R.found && qg >= qacc && qg < qacc + nq) {
+      const long long gi = qg - qacc;
+      R.s = s; R.b = b; R.g = (int)(gi / MP); R.mp = (int)(gi % MP); R.tiles = tiles;
+      R.start = acc + gi * tiles;
+      R.found = true;
+    }
+    acc += nq * tiles;
+    qacc += nq;
+  }
+  R.T = acc;
+  return R;
+}
+
 // Ancestor-or-self bit mask of tree node i (local id) over local ids 0..127:
 // mask bit c set iff node c is i or an ancestor of i.  Returns false if a parent id
 // met on the walk is outside [-1, node) (then only i's own bit is set).

@@ -101,8 +101,9 @@ tva_status make_layout(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
   pr.kv_capacity = kv_cap; pr.node_capacity = node_cap;
   const long long groups = (long long)B * Hkv * ((max_nodes + W * npt - 1) / (W * npt));
   L->slots = pr.U + groups;
-  L->o_bytes = align256((size_t)L->slots * pr.RG * d * sizeof(float));
-  L->lse_bytes = align256((size_t)L->slots * pr.RG * sizeof(float));
+  const size_t rgp = (size_t)W * 128;  // padded rows per slot (see o_part_offset)
+  L->o_bytes = align256((size_t)L->slots * rgp * d * sizeof(float));
+  L->lse_bytes = align256((size_t)L->slots * rgp * sizeof(float));
   L->total = L->o_bytes + L->lse_bytes;
   return TVA_OK;
 }
