@@ -26,10 +26,9 @@ namespace tva {
 namespace {
 
 constexpr int kCuCap = 2048;      // ints of shared memory for the staged cu_* arrays
-constexpr int kWarpsPerBlock = 2;
 
-template <typename T, int D, int CG, int NB>
-__global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(CombineArgs a) {
+template <typename T, int D, int CG, int NB, int WPB>
+__global__ void __launch_bounds__(32 * WPB) combine_kernel(CombineArgs a) {
   constexpr int NCG = D / 4 / CG;  // column-group sets per row block
   __shared__ int cu_buf[kCuCap];
   Problem pr = a.pr;
@@ -38,7 +37,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) combine_kernel(CombineArg
   const int MT = mtile_rows(pr.G);
   const int W = pr.RG / MT;
   const int RGP = W * 128;
-  const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const long long wid = (long long)blockIdx.x * WPB + (threadIdx.x >> 5);
   const long long per_group = (long long)(RGP / 32) * NCG;
   const long long qg = wid / per_group;
   const int rb = (int)(wid % per_group) / NCG;  // 32-row block
@@ -137,14 +136,16 @@ long long max_row_groups(const Problem& pr) {
   return (long long)pr.B * pr.Hkv * (((long long)pr.max_nodes * pr.G + pr.RG - 1) / pr.RG);
 }
 
+// WPB warps per block: as many as keep the registers of two blocks per SM or more.
 template <typename T, int D, int CG, int NB>
 cudaError_t launch_typed(const CombineArgs& a, cudaStream_t s) {
+  constexpr int WPB = CG == 1 ? 8 : 4;
   const int RGP = padded_group_rows(a.pr.RG, a.pr.G);
   const long long warps = max_row_groups(a.pr) * (RGP / 32) * (D / 4 / CG);
-  const long long blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  const long long blocks = (warps + WPB - 1) / WPB;
   if (blocks <= 0) return cudaSuccess;
-  return check_cuda(launch_pdl(combine_kernel<T, D, CG, NB>, dim3((unsigned)blocks),
-                               dim3(32 * kWarpsPerBlock), 0, s, a),
+  return check_cuda(launch_pdl(combine_kernel<T, D, CG, NB, WPB>, dim3((unsigned)blocks), dim3(32 * WPB), 0,
+                               s, a),
                     "launch combine_kernel");
 }
 
