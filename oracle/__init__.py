@@ -15,6 +15,7 @@ definition.
 * :mod:`oracle.lse_merge` - the log-sum-exp aggregation of attention partials.
 * :mod:`oracle.acceptance` - the greedy longest-accepted-path walk.
 * :mod:`oracle.expected_tokens` - expected tokens per verification cycle.
+* :mod:`oracle.kv_commit` - committing the accepted path's K/V into the cache.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against facts fixed by the pages
 or by mathematics (closed forms, brute force, library routines on independently
@@ -24,6 +25,7 @@ from .tree_attention import ancestor_mask, tree_verify_attention, tree_verify_at
 from .lse_merge import merge_partials, attention_partial
 from .acceptance import accept_longest_path
 from .expected_tokens import expected_tokens, survival_from_conditional, iid_expected_tokens
+from .kv_commit import commit_accepted_kv
 
 __all__ = [
     "ancestor_mask",
@@ -35,4 +37,5 @@ __all__ = [
     "expected_tokens",
     "survival_from_conditional",
     "iid_expected_tokens",
+    "commit_accepted_kv",
 ]

@@ -230,3 +230,105 @@ def chain_expected_tokens_by_enumeration(accept_fn, conditional):
         alen, _, _ = accept_fn(parent, draft, slot, np.array([0, gamma], np.int32))
         total += pr * (int(alen[0]) + 1)
     return total
+
+
+# ----------------------------------------------------------------------------- KV commit
+def commit_problem(rng, B=3, Hq=4, Hkv=2, d=8, max_m=7, room=9):
+    """A batch of random trees plus a cache in which sequence b owns rows
+    [base_b, base_b + P_b + room): its prefix, then reserved room filled with junk.
+    One node per sequence is picked and its root->node path (from the parent array)
+    is the path to commit; dst_row[b] = base_b + P_b."""
+    Ps = [int(rng.integers(0, 12)) for _ in range(B)]
+    ms = [int(rng.integers(1, max_m + 1)) for _ in range(B)]
+    parents, paths = [], []
+    for m in ms:
+        par = np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, m)], dtype=np.int32)
+        parents.append(par)
+        paths.append(path_to(par, int(rng.integers(0, m))))
+    N = sum(ms)
+    cu_nodes = np.concatenate([[0], np.cumsum(ms)]).astype(np.int32)
+    cu_prefix = np.concatenate([[0], np.cumsum(Ps)]).astype(np.int32)
+    kc = rng.standard_normal((int(cu_prefix[-1]), Hkv, d))
+    vc = rng.standard_normal((int(cu_prefix[-1]), Hkv, d))
+    base = np.concatenate([[0], np.cumsum([P + room for P in Ps])]).astype(np.int64)
+    k_res = rng.standard_normal((int(base[-1]), Hkv, d))     # junk in the reserved room
+    v_res = rng.standard_normal((int(base[-1]), Hkv, d))
+    for b in range(B):
+        k_res[base[b]:base[b] + Ps[b]] = kc[cu_prefix[b]:cu_prefix[b + 1]]
+        v_res[base[b]:base[b] + Ps[b]] = vc[cu_prefix[b]:cu_prefix[b + 1]]
+    accept_len = np.array([len(p) for p in paths], dtype=np.int32)
+    accept_path = np.full(N, -1, dtype=np.int32)
+    for b, p in enumerate(paths):
+        accept_path[cu_nodes[b]:cu_nodes[b] + len(p)] = p
+    return dict(q=rng.standard_normal((N, Hq, d)), k_cache=kc, v_cache=vc,
+                tree_k=rng.standard_normal((N, Hkv, d)), tree_v=rng.standard_normal((N, Hkv, d)),
+                parent=np.concatenate(parents).astype(np.int32), cu_prefix=cu_prefix, cu_nodes=cu_nodes,
+                num_kv_heads=Hkv, k_res=k_res, v_res=v_res, base=base, Ps=Ps,
+                accept_len=accept_len, accept_path=accept_path,
+                dst_row=(base[:-1] + np.array(Ps)).astype(np.int32))
+
+
+def _commit(commit_fn, pr):
+    return commit_fn(pr["k_res"], pr["v_res"], pr["tree_k"], pr["tree_v"], pr["cu_nodes"],
+                     pr["accept_len"], pr["accept_path"], pr["dst_row"])
+
+
+def check_commit_causal(commit_fn, attn_fn, rng, trials=6):
+    """After committing the path root -> i, causal attention at every position of the
+    new sequence (prefix ++ committed rows) equals tree attention for the path node
+    there: tree attention lets a node see the prefix, its ancestors and itself, and the
+    committed sequence is exactly that, in order."""
+    for _ in range(trials):
+        pr = commit_problem(rng)
+        out_t, _ = attn_fn(**{k: pr[k] for k in ("q", "k_cache", "v_cache", "tree_k", "tree_v", "parent",
+                                                 "cu_prefix", "cu_nodes", "num_kv_heads")})
+        k_new, v_new = _commit(commit_fn, pr)
+        Hq, Hkv = pr["q"].shape[1], pr["num_kv_heads"]
+        G = Hq // Hkv
+        for b in range(len(pr["Ps"])):
+            n0, L = int(pr["cu_nodes"][b]), int(pr["accept_len"][b])
+            rows = slice(int(pr["base"][b]), int(pr["dst_row"][b]) + L)
+            K = torch.from_numpy(k_new[rows]).permute(1, 0, 2).repeat_interleave(G, 0)   # [Hq, S, d]
+            V = torch.from_numpy(v_new[rows]).permute(1, 0, 2).repeat_interleave(G, 0)
+            S = K.shape[1]
+            for j in range(L):
+                node = n0 + int(pr["accept_path"][n0 + j])
+                pos = S - L + j                              # the node's position
+                qt = torch.from_numpy(pr["q"][node])[:, None, :]
+                o = F.scaled_dot_product_attention(qt, K[:, :pos + 1], V[:, :pos + 1])[:, 0].numpy()
+                np.testing.assert_allclose(o, out_t[node], rtol=1e-11, atol=1e-11)
+
+
+def check_commit_touches_only_the_path_rows(commit_fn, rng, trials=4):
+    for _ in range(trials):
+        pr = commit_problem(rng)
+        k_new, v_new = _commit(commit_fn, pr)
+        keep = np.ones(len(k_new), dtype=bool)
+        for b in range(len(pr["Ps"])):
+            keep[int(pr["dst_row"][b]):int(pr["dst_row"][b]) + int(pr["accept_len"][b])] = False
+        np.testing.assert_array_equal(k_new[keep], pr["k_res"][keep])
+        np.testing.assert_array_equal(v_new[keep], pr["v_res"][keep])
+
+
+def check_commit_empty_path_writes_nothing(commit_fn, rng):
+    pr = commit_problem(rng)
+    pr["accept_len"][:] = 0
+    pr["accept_path"][:] = -1
+    k_new, v_new = _commit(commit_fn, pr)
+    np.testing.assert_array_equal(k_new, pr["k_res"])
+    np.testing.assert_array_equal(v_new, pr["v_res"])
+
+
+def check_commit_full_chain(commit_fn, rng, m=6):
+    """A chain accepted to its end commits the tree rows themselves, in order."""
+    pr = commit_problem(rng, B=1, max_m=1)
+    N = m
+    pr["tree_k"] = rng.standard_normal((N, pr["num_kv_heads"], pr["k_res"].shape[2]))
+    pr["tree_v"] = rng.standard_normal((N, pr["num_kv_heads"], pr["k_res"].shape[2]))
+    pr["cu_nodes"] = np.array([0, m], dtype=np.int32)
+    pr["accept_len"] = np.array([m], dtype=np.int32)
+    pr["accept_path"] = np.arange(m, dtype=np.int32)
+    k_new, v_new = _commit(commit_fn, pr)
+    d0 = int(pr["dst_row"][0])
+    np.testing.assert_array_equal(k_new[d0:d0 + m], pr["tree_k"])
+    np.testing.assert_array_equal(v_new[d0:d0 + m], pr["tree_v"])

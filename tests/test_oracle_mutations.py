@@ -147,3 +147,61 @@ def test_walk_copy_without_mistakes_passes():
 @pytest.mark.parametrize("mistake", [dict(tie_later=True), dict(own_slot=True), dict(bonus_shift=0)])
 def test_acceptance_mutants_are_caught(mistake):
     assert _accept_pins_fail(lambda *a: _walk_variant(*a, **mistake)) > 0
+
+
+# ----------------------------------------------------------------------------- KV commit
+def _commit_pins_fail(fn):
+    checks = [
+        lambda: _pins.check_commit_causal(fn, tree_verify_attention, np.random.default_rng(21)),
+        lambda: _pins.check_commit_touches_only_the_path_rows(fn, np.random.default_rng(22)),
+        lambda: _pins.check_commit_empty_path_writes_nothing(fn, np.random.default_rng(23)),
+        lambda: _pins.check_commit_full_chain(fn, np.random.default_rng(24)),
+    ]
+    failed = 0
+    for c in checks:
+        try:
+            c()
+        except (AssertionError, IndexError, ValueError):
+            failed += 1
+    return failed
+
+
+def _commit_mutant(src_of, dst_of, copy_v=True):
+    """The oracle's loop with the source row, destination row or V copy altered."""
+    def fn(k_cache, v_cache, tree_k, tree_v, cu_nodes, accept_len, accept_path, dst_row):
+        k_out, v_out = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+        for b in range(len(cu_nodes) - 1):
+            n0, L = int(cu_nodes[b]), int(accept_len[b])
+            for j in range(L):
+                s = src_of(accept_path, n0, j, L)
+                t = dst_of(dst_row, b, j)
+                k_out[t] = tree_k[s]
+                if copy_v:
+                    v_out[t] = tree_v[s]
+        return k_out, v_out
+    return fn
+
+
+def test_real_commit_oracle_passes_all_commit_pins():
+    from oracle import commit_accepted_kv
+    assert _commit_pins_fail(commit_accepted_kv) == 0
+
+
+def test_commit_mutant_leaf_first():
+    fn = _commit_mutant(lambda ap, n0, j, L: n0 + int(ap[n0 + L - 1 - j]), lambda d, b, j: int(d[b]) + j)
+    assert _commit_pins_fail(fn) > 0
+
+
+def test_commit_mutant_destination_off_by_one():
+    fn = _commit_mutant(lambda ap, n0, j, L: n0 + int(ap[n0 + j]), lambda d, b, j: int(d[b]) + j + 1)
+    assert _commit_pins_fail(fn) > 0
+
+
+def test_commit_mutant_local_id_used_as_global_row():
+    fn = _commit_mutant(lambda ap, n0, j, L: int(ap[n0 + j]), lambda d, b, j: int(d[b]) + j)
+    assert _commit_pins_fail(fn) > 0
+
+
+def test_commit_mutant_values_not_copied():
+    fn = _commit_mutant(lambda ap, n0, j, L: n0 + int(ap[n0 + j]), lambda d, b, j: int(d[b]) + j, copy_v=False)
+    assert _commit_pins_fail(fn) > 0
