@@ -350,6 +350,33 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, k1 = float(t[0]), float(t[1])
 
+    # ---- KV commit of the accepted path (a "next" row, measured on its own, outside the
+    # step): the step's own acceptance result, appended to a reserved cache region.
+    room = int(w.tree_sizes.max())
+    k_dst = torch.zeros((B * room,) + tuple(d["k_cache"].shape[1:]), dtype=d["k_cache"].dtype, device=dev)
+    v_dst = torch.zeros_like(k_dst)
+    dst_row = torch.arange(0, B * room, room, dtype=torch.int32, device=dev)
+
+    def commit():
+        api.commit_accepted_kv(d["cu_nodes"], alen, apath, d["tree_k"], d["tree_v"], dst_row, k_dst, v_dst,
+                               max_nodes=max_nodes, dev_status=status)
+
+    accept(d)
+    for _ in range(args.warmup):
+        commit()
+    torch.cuda.synchronize()
+    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda._sleep(int(20e6))
+    for i in range(K):
+        flush.fill_((i + 3) & 0xFF)
+        evc[i][0].record(stream)
+        commit()
+        evc[i][1].record(stream)
+    torch.cuda.synchronize()
+    commit_ms = float(np.mean([evc[i][0].elapsed_time(evc[i][1]) for i in range(K)]))
+    committed_rows = int(alen.sum().item())
+    commit_bytes = 2 * 2 * committed_rows * w.num_kv_heads * w.head_dim * (2 if w.dtype == "bf16" else 4)
+
     # ---- end to end through the public API from pinned host buffers
     pinned = {k: v.pin_memory() for k, v in host.items()}
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -456,6 +483,9 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "kv_commit": {"us_per_launch": commit_ms * 1e3, "rows": committed_rows, "bytes": commit_bytes,
+                      "gbs": commit_bytes / (commit_ms * 1e-3) / 1e9,
+                      "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }

@@ -182,6 +182,34 @@ tva_status accept_longest_path(int batch, int node_capacity, const int32_t* cu_n
                                int32_t* accept_len, int32_t* accept_path,
                                int32_t* next_token, int32_t* dev_status, void* stream);
 
+/* Commits each sequence's accepted path into the K/V cache ("Faster decoding", "The
+ * scheduler must plan speculative work": after verification only the target KV of the
+ * accepted draft prefix is committed and rejected branches are released).  The pages
+ * give no interface; this one takes the acceptance walk's outputs as they are.
+ *   batch, num_kv_heads, head_dim (64 or 128), dtype: as for the attention
+ *   node_capacity rows in tree_k / tree_v [node_capacity, Hkv, d] (the tree nodes' K / V)
+ *   max_nodes     bound on every m_b (<= 128; sizes the launch; a larger m_b is an
+ *                 out-of-bounds sequence, see below)
+ *   kv_capacity   rows in k_cache / v_cache [kv_capacity, Hkv, d]
+ *   cu_nodes      [B+1] device, as in tva_params
+ *   accept_len [B], accept_path [N]: as written by accept_longest_path
+ *   dst_row       [B] device int32: first cache row for sequence b's committed rows
+ *                 (for a cache whose sequences own reserved room after their prefix,
+ *                 the prefix end)
+ * Row j < accept_len[b] of the path (root first) is copied: K and V of tree row
+ * cu_nodes[b] + accept_path[cu_nodes[b] + j] go to cache row dst_row[b] + j, bit for
+ * bit.  No other cache row is written.  All pointers are device pointers; tree_k, tree_v,
+ * k_cache and v_cache are 16-byte aligned and the sources must not overlap the
+ * destination buffers (TVA_ERR_INVALID_ARG from the host, nothing launched).  A
+ * sequence whose node range, path length, path ids or destination range is out of
+ * bounds is left untouched and TVA_ERR_INVALID_ARG goes to *dev_status.  Ordered on
+ * `stream` after the acceptance walk that wrote accept_len / accept_path. */
+tva_status commit_accepted_kv(int batch, int num_kv_heads, int head_dim, tva_dtype dtype, int node_capacity,
+                              int max_nodes, long long kv_capacity, const int32_t* cu_nodes,
+                              const int32_t* accept_len, const int32_t* accept_path, const void* tree_k,
+                              const void* tree_v, const int32_t* dst_row, void* k_cache, void* v_cache,
+                              int32_t* dev_status, void* stream);
+
 /* Description of the last host-side CUDA or driver failure seen by this thread
  * (the call that failed and its error string), "" if none.  Thread-local storage,
  * valid until the thread's next failing call. */

@@ -34,7 +34,8 @@ def test_header_declares_the_expected_entry_points():
     names = _declared_functions()
     for n in ("tree_verify_attn_varlen", "tree_verify_attn", "accept_longest_path",
               "tva_workspace_size", "tree_verify_attn_partials", "tree_verify_attn_combine",
-              "tva_status_string", "tva_release", "tva_read_device_status", "tva_num_workers"):
+              "tva_status_string", "tva_release", "tva_read_device_status", "tva_num_workers",
+              "commit_accepted_kv"):
         assert n in names
 
 
@@ -85,3 +86,23 @@ def test_host_checks_reject_null_and_misaligned_pointers(lib):
     assert lib.accept_longest_path(0, 8, a, a, a, a, a, a, a, a, None) == 1
     assert lib.accept_longest_path(2, 8, a, None, a, a, a, a, a, a, None) == 1
     assert lib.accept_longest_path(2, -1, a, a, a, a, a, a, a, a, None) == 1
+
+
+def test_commit_rejects_bad_arguments_on_the_host(lib):
+    """Host-side checks return TVA_ERR_INVALID_ARG before anything is launched (the
+    pointers below are never dereferenced)."""
+    P = ctypes.c_void_p
+    a = 1 << 20          # fake, 16-byte aligned device addresses
+    row = 8 * 128 * 2    # Hkv=8, d=128, bf16
+
+    def call(batch=1, hkv=8, d=128, dtype=0, ncap=16, maxn=16, kvcap=64, tk=a, tv=a + 16 * row,
+             kc=a + 64 * row, vc=a + 256 * row):
+        return lib.commit_accepted_kv(batch, hkv, d, dtype, ncap, maxn, kvcap, P(8), P(8), P(8), P(tk), P(tv),
+                                      P(8), P(kc), P(vc), P(8), None)
+    assert call(batch=0) == 1
+    assert call(d=96) == 1
+    assert call(dtype=7) == 1
+    assert call(maxn=0) == 1 and call(maxn=129) == 1
+    assert call(tk=a + 8) == 1                       # misaligned
+    assert call(kc=a + 8 * row) == 1                 # k_cache overlaps tree_k
+    assert call(vc=a + 64 * row + 10 * row) == 1     # v_cache overlaps k_cache

@@ -69,6 +69,8 @@ def load_library(path: str | None = None):
         "tva_read_device_status": (_I, [ctypes.POINTER(ctypes.c_int32), _P]),
         "tva_release": (None, []),
         "accept_longest_path": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "commit_accepted_kv": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_longlong, _P, _P, _P, _P, _P, _P, _P, _P,
+                                    _P, _P]),
         "tva_status_string": (ctypes.c_char_p, [_I]),
         "tva_last_error": (ctypes.c_char_p, []),
     }
@@ -247,6 +249,33 @@ def accept_longest_path(cu_nodes, parent, draft_tok, target_argmax, accept_len=N
         _ptr(accept_path), _ptr(next_token), _ptr(dev_status), _stream(stream))
     _check(code, "accept_longest_path")
     return accept_len, accept_path, next_token
+
+
+def commit_accepted_kv(cu_nodes, accept_len, accept_path, tree_k, tree_v, dst_row, k_cache, v_cache,
+                       max_nodes=None, dev_status=None, stream=None):
+    """Copies each sequence's accepted path (root first) of tree_k / tree_v [N, Hkv, d]
+    into k_cache / v_cache [rows, Hkv, d] at rows dst_row[b] .. dst_row[b] +
+    accept_len[b] - 1, in place.  Returns dev_status (int32 [1], 0 = ok)."""
+    for name, t in (("cu_nodes", cu_nodes), ("accept_len", accept_len), ("accept_path", accept_path),
+                    ("dst_row", dst_row)):
+        _dev(t, name, torch.int32)
+    _dev(tree_k, "tree_k")
+    for name, t in (("tree_v", tree_v), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, name, tree_k.dtype)
+    if tree_k.dtype not in DTYPES:
+        raise TypeError(f"unsupported dtype {tree_k.dtype}")
+    B = cu_nodes.numel() - 1
+    N, Hkv, d = tree_k.shape
+    if max_nodes is None:
+        max_nodes = int((cu_nodes[1:] - cu_nodes[:-1]).max().item()) if B > 0 else 1
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=tree_k.device)
+    code = load_library().commit_accepted_kv(
+        B, Hkv, d, DTYPES[tree_k.dtype], N, max(1, int(max_nodes)), k_cache.shape[0], _ptr(cu_nodes),
+        _ptr(accept_len), _ptr(accept_path), _ptr(tree_k), _ptr(tree_v), _ptr(dst_row), _ptr(k_cache),
+        _ptr(v_cache), _ptr(dev_status), _stream(stream))
+    _check(code, "commit_accepted_kv")
+    return dev_status
 
 
 def tree_verify_attn_varlen_noalloc(q, k_cache, v_cache, tree_k, tree_v, parent, cu_prefix, cu_nodes,

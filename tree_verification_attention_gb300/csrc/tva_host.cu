@@ -349,4 +349,38 @@ tva_status accept_longest_path(int batch, int node_capacity, const int32_t* cu_n
                                                                                  : TVA_ERR_CUDA;
 }
 
+tva_status commit_accepted_kv(int batch, int num_kv_heads, int head_dim, tva_dtype dtype, int node_capacity,
+                              int max_nodes, long long kv_capacity, const int32_t* cu_nodes,
+                              const int32_t* accept_len, const int32_t* accept_path, const void* tree_k,
+                              const void* tree_v, const int32_t* dst_row, void* k_cache, void* v_cache,
+                              int32_t* dev_status, void* stream) {
+  if (batch < 1 || num_kv_heads < 1 || (head_dim != 64 && head_dim != 128) ||
+      (dtype != TVA_BF16 && dtype != TVA_FP32) || node_capacity < 0 || max_nodes < 1 ||
+      max_nodes > tva::kMaxNodes || kv_capacity < 0 || !cu_nodes || !accept_len || !accept_path || !tree_k ||
+      !tree_v || !dst_row || !k_cache || !v_cache || !dev_status)
+    return TVA_ERR_INVALID_ARG;
+  if (!aligned16(tree_k) || !aligned16(tree_v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return TVA_ERR_INVALID_ARG;
+  const size_t row = (size_t)num_kv_heads * head_dim * (dtype == TVA_BF16 ? 2 : 4);
+  // The copy has no defined order, so no source row may alias a destination row; the
+  // buffers are compared over their full extents.
+  auto overlap = [](const void* x, size_t nx, const void* y, size_t ny) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(x), b0 = reinterpret_cast<uintptr_t>(y);
+    return nx > 0 && ny > 0 && a0 < b0 + ny && b0 < a0 + nx;
+  };
+  const size_t nsrc = (size_t)node_capacity * row, ndst = (size_t)kv_capacity * row;
+  if (overlap(tree_k, nsrc, k_cache, ndst) || overlap(tree_k, nsrc, v_cache, ndst) ||
+      overlap(tree_v, nsrc, k_cache, ndst) || overlap(tree_v, nsrc, v_cache, ndst) ||
+      overlap(k_cache, ndst, v_cache, ndst))
+    return TVA_ERR_INVALID_ARG;
+  tva::CommitArgs a;
+  a.B = batch; a.row_bytes = (int)row; a.node_capacity = node_capacity; a.max_nodes = max_nodes;
+  a.kv_capacity = kv_capacity;
+  a.cu_nodes = cu_nodes; a.accept_len = accept_len; a.accept_path = accept_path;
+  a.tree_k = tree_k; a.tree_v = tree_v; a.dst_row = dst_row; a.k_cache = k_cache; a.v_cache = v_cache;
+  a.status = dev_status;
+  return tva::launch_commit(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TVA_OK
+                                                                                            : TVA_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -48,6 +48,23 @@ struct AcceptArgs {
   int32_t* status;
 };
 
+struct CommitArgs {
+  int B;
+  int row_bytes;            // bytes of one node's K (or V) row: Hkv * d * element size
+  int node_capacity;
+  int max_nodes;            // bound on every m_b (<= kMaxNodes); sizes the grid
+  long long kv_capacity;
+  const int32_t* cu_nodes;
+  const int32_t* accept_len;
+  const int32_t* accept_path;
+  const void* tree_k;
+  const void* tree_v;
+  const int32_t* dst_row;
+  void* k_cache;
+  void* v_cache;
+  int32_t* status;
+};
+
 // Records a host-side failure for tva_last_error() (thread-local).
 void record_error(const char* where, int code, const char* what);
 // Records `e` (if it is an error) and returns it unchanged.
@@ -79,5 +96,6 @@ cudaError_t launch_partials_simt(const PartialArgs& a, int dtype, cudaStream_t s
 cudaError_t launch_partials_tc(const PartialArgs& a, int W, int npt, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
 
 }  // namespace tva
