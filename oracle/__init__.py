@@ -16,6 +16,7 @@ definition.
 * :mod:`oracle.acceptance` - the greedy longest-accepted-path walk.
 * :mod:`oracle.expected_tokens` - expected tokens per verification cycle.
 * :mod:`oracle.kv_commit` - committing the accepted path's K/V into the cache.
+* :mod:`oracle.rejection_sampling` - stochastic verification of a draft chain.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against facts fixed by the pages
 or by mathematics (closed forms, brute force, library routines on independently
@@ -26,6 +27,7 @@ from .lse_merge import merge_partials, attention_partial
 from .acceptance import accept_longest_path
 from .expected_tokens import expected_tokens, survival_from_conditional, iid_expected_tokens
 from .kv_commit import commit_accepted_kv
+from .rejection_sampling import verify_chain_sampling, quantised_draw
 
 __all__ = [
     "ancestor_mask",
@@ -38,4 +40,6 @@ __all__ = [
     "survival_from_conditional",
     "iid_expected_tokens",
     "commit_accepted_kv",
+    "verify_chain_sampling",
+    "quantised_draw",
 ]

@@ -332,3 +332,109 @@ def check_commit_full_chain(commit_fn, rng, m=6):
     d0 = int(pr["dst_row"][0])
     np.testing.assert_array_equal(k_new[d0:d0 + m], pr["tree_k"])
     np.testing.assert_array_equal(v_new[d0:d0 + m], pr["tree_v"])
+
+
+# ----------------------------------------------------------------- stochastic verification
+def sampling_case(kind, V=6, rng=None):
+    """(p, q) float32 rows of one position for the Faster decoding test list: p == q,
+    partially overlapping supports, disjoint supports."""
+    rng = rng or np.random.default_rng(0)
+    if kind == "equal":
+        p = rng.random(V) + 0.05
+        q = p.copy()
+    elif kind == "partial":
+        p = rng.random(V) + 0.05
+        q = rng.random(V) + 0.05
+        p[: V // 3] = 0.0          # q has mass where p has none, and vice versa
+        q[-(V // 3):] = 0.0
+    elif kind == "disjoint":
+        p = np.zeros(V)
+        q = np.zeros(V)
+        p[: V // 2] = rng.random(V // 2) + 0.05
+        q[V // 2:] = rng.random(V - V // 2) + 0.05
+    else:
+        raise ValueError(kind)
+    p = (p / p.sum()).astype(np.float32)
+    q = (q / q.sum()).astype(np.float32)
+    return p, q
+
+
+def draw_chain(rng, ps, qs, n):
+    """n independent rounds of one chain: ps [gamma+1, V], qs [gamma, V] (the same for
+    every round).  Draft tokens X_i ~ q_i, uniforms in [0, 1) float32."""
+    gamma, V = qs.shape
+    w = qs.astype(np.float64)
+    w /= w.sum(1, keepdims=True)
+    draft = np.stack([rng.choice(V, size=n, p=w[i]) for i in range(gamma)], 1)
+    p = np.tile(ps, (n, 1))
+    q = np.tile(qs, (n, 1))
+    u_acc = rng.random((n, gamma)).astype(np.float32)
+    u_smp = rng.random(n).astype(np.float32)
+    cu = np.arange(0, (n + 1) * gamma, gamma, dtype=np.int32)
+    return p, q, draft.reshape(-1).astype(np.int32), u_acc.reshape(-1), u_smp, cu
+
+
+def emitted(draft, accept_len, out_token, gamma):
+    """Tokens emitted by each round: the accepted drafts, then the correction / bonus."""
+    d = draft.reshape(-1, gamma)
+    return [list(d[r, :accept_len[r]]) + [int(out_token[r])] for r in range(len(accept_len))]
+
+
+def assert_freq(tokens, p, what):
+    """Empirical frequencies within 5 standard errors of p (plus 1e-3)."""
+    tokens = np.asarray(tokens)
+    n = len(tokens)
+    assert n > 500, (what, n)
+    f = np.bincount(tokens, minlength=len(p)) / n
+    se = np.sqrt(np.maximum(p * (1 - p), 1e-12) / n)
+    bad = np.abs(f - p) > 5 * se + 1e-3
+    assert not bad.any(), (what, f, p)
+
+
+def check_sampling_marginals(verify_fn, rng, n=40000):
+    """gamma = 2, three positions with different (p, q): the first emitted token ~ p_1;
+    given the first draft was accepted, the second ~ p_2; given both were accepted, the
+    bonus ~ p_3 - for p == q, partial overlap and disjoint supports."""
+    for kind in ("equal", "partial", "disjoint"):
+        rows = [sampling_case(kind, rng=np.random.default_rng(s)) for s in (1, 2)]
+        ps = np.stack([rows[0][0], rows[1][0], sampling_case("equal", rng=np.random.default_rng(3))[0]])
+        qs = np.stack([rows[0][1], rows[1][1]])
+        p, q, draft, ua, us, cu = draw_chain(rng, ps, qs, n)
+        alen, out = verify_fn(p, q, draft, ua, us, cu)
+        em = emitted(draft, alen, out, 2)
+        assert_freq([e[0] for e in em], ps[0].astype(np.float64), (kind, "token 1"))
+        if kind != "disjoint":
+            assert_freq([e[1] for e in em if len(e) > 1], ps[1].astype(np.float64), (kind, "token 2"))
+        if kind == "equal":
+            assert_freq([e[2] for e in em if len(e) > 2], ps[2].astype(np.float64), (kind, "bonus"))
+
+
+def check_sampling_forced_cases(verify_fn, rng, n=3000):
+    """Forced first rejection, late rejection and all-accept (Faster decoding, test list)."""
+    V, gamma = 6, 4
+    same, _ = sampling_case("equal", V, np.random.default_rng(4))
+    dp, dq = sampling_case("disjoint", V, np.random.default_rng(5))
+    for k in range(gamma + 1):        # positions < k have p == q, position k disjoint supports
+        ps = np.stack([same] * k + [dp] * (gamma - k) + [same]).astype(np.float32)
+        qs = np.stack([same] * k + [dq] * (gamma - k)).astype(np.float32)
+        p, q, draft, ua, us, cu = draw_chain(rng, ps, qs, n)
+        alen, out = verify_fn(p, q, draft, ua, us, cu)
+        assert (alen == k).all(), (k, np.bincount(alen))
+        # the correction comes from the residual, here p itself (disjoint supports)
+        assert_freq(out, (dp if k < gamma else same).astype(np.float64), ("forced", k))
+
+
+def check_quantised_draw_against_searchsorted(draw_fn, rng, trials=300):
+    """Away from the cumulative boundaries the quantised draw is the plain inverse CDF."""
+    for _ in range(trials):
+        V = int(rng.integers(1, 40))
+        w = rng.random(V).astype(np.float32)
+        w[rng.random(V) < 0.3] = 0
+        if w.sum() == 0:
+            w[0] = 1
+        u = np.float32(rng.random())
+        c = np.cumsum(w.astype(np.float64))
+        t = np.float64(u) * c[-1]
+        if np.min(np.abs(c - t)) < 1e-6 * c[-1]:
+            continue
+        assert draw_fn(w, u) == int(np.searchsorted(c, t, side="right"))

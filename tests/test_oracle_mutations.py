@@ -205,3 +205,79 @@ def test_commit_mutant_local_id_used_as_global_row():
 def test_commit_mutant_values_not_copied():
     fn = _commit_mutant(lambda ap, n0, j, L: n0 + int(ap[n0 + j]), lambda d, b, j: int(d[b]) + j, copy_v=False)
     assert _commit_pins_fail(fn) > 0
+
+
+# ----------------------------------------------------------------- stochastic verification
+def _sampling_pins_fail(fn):
+    checks = [
+        lambda: _pins.check_sampling_marginals(fn, np.random.default_rng(41), n=20000),
+        lambda: _pins.check_sampling_forced_cases(fn, np.random.default_rng(42), n=1500),
+    ]
+    failed = 0
+    for c in checks:
+        try:
+            c()
+        except (AssertionError, ValueError, IndexError):
+            failed += 1
+    return failed
+
+
+def _sampling_mutant(accept=None, resid=None, bonus_row=0, stop=True):
+    """The oracle's loop with one rule altered."""
+    from oracle import quantised_draw
+
+    def fn(p, q, draft_tok, u_accept, u_sample, cu_draft):
+        p = np.asarray(p, np.float32); q = np.asarray(q, np.float32)
+        B = len(cu_draft) - 1
+        alen = np.zeros(B, np.int32); out = np.zeros(B, np.int32)
+        for b in range(B):
+            g0, gamma = int(cu_draft[b]), int(cu_draft[b + 1] - cu_draft[b])
+            k, first_rej = 0, None
+            for i in range(gamma):
+                x = int(draft_tok[g0 + i]); px, qx = p[g0 + b + i, x], q[g0 + i, x]
+                u = np.float32(u_accept[g0 + i])
+                ok = accept(px, qx, u) if accept else (px >= qx or np.float32(u * qx) < px)
+                if ok:
+                    k += 1              # (past a rejection only when the mutant does not stop)
+                else:
+                    if first_rej is None:
+                        first_rej = i
+                    if stop:
+                        break
+            alen[b] = k
+            j = first_rej if first_rej is not None else gamma
+            prow = p[g0 + b + j]
+            if first_rej is not None:
+                w = resid(prow, q[g0 + j]) if resid else np.maximum(np.float32(0), prow - q[g0 + j])
+                t = quantised_draw(np.maximum(w, 0), u_sample[b])
+                out[b] = t if t >= 0 else quantised_draw(prow, u_sample[b])
+            else:
+                out[b] = quantised_draw(p[g0 + b + j - bonus_row], u_sample[b])
+        return alen, out
+    return fn
+
+
+def test_real_sampling_oracle_passes_its_pins():
+    from oracle import verify_chain_sampling
+    assert _sampling_pins_fail(verify_chain_sampling) == 0
+    assert _sampling_pins_fail(_sampling_mutant()) == 0      # the mutant frame itself is faithful
+
+
+def test_sampling_mutant_accept_test_reversed():
+    assert _sampling_pins_fail(_sampling_mutant(accept=lambda px, qx, u: np.float32(u * qx) > px)) > 0
+
+
+def test_sampling_mutant_correction_from_p():
+    assert _sampling_pins_fail(_sampling_mutant(resid=lambda pr, qr: pr)) > 0
+
+
+def test_sampling_mutant_residual_reversed():
+    assert _sampling_pins_fail(_sampling_mutant(resid=lambda pr, qr: np.maximum(0, qr - pr))) > 0
+
+
+def test_sampling_mutant_bonus_from_the_last_draft_position():
+    assert _sampling_pins_fail(_sampling_mutant(bonus_row=1)) > 0
+
+
+def test_sampling_mutant_accepts_past_the_first_rejection():
+    assert _sampling_pins_fail(_sampling_mutant(stop=False)) > 0
