@@ -210,6 +210,37 @@ tva_status commit_accepted_kv(int batch, int num_kv_heads, int head_dim, tva_dty
                               const void* tree_v, const int32_t* dst_row, void* k_cache, void* v_cache,
                               int32_t* dev_status, void* stream);
 
+/* Stochastic verification of draft chains by modified rejection sampling ("Faster
+ * decoding", "Modified rejection sampling keeps the target distribution"): left to
+ * right, draft token x at a position is accepted with probability min(1, p(x)/q(x));
+ * the first rejection ends the round with a correction token drawn from the residual
+ * [p - q]_+ / Z; if all gamma drafts are accepted a bonus token is drawn from p at the
+ * next position.  The pages give no interface; the random numbers are inputs.
+ *   batch, vocab   B sequences over a vocabulary of V tokens
+ *   max_draft      bound on every gamma_b (validated on the device)
+ *   cu_draft       [B+1] device int32: sequence b's draft positions are
+ *                  cu_draft[b] .. cu_draft[b+1]-1 (gamma_b of them)
+ *   p              [p_rows, V] fp32 target probabilities; sequence b owns the gamma_b + 1
+ *                  rows cu_draft[b] + b .. cu_draft[b+1] + b (the last is the bonus
+ *                  position)
+ *   q              [q_rows, V] fp32 draft probabilities, one row per draft position
+ *   draft_tok      [sum gamma_b] int32, each drawn from its q row (q(x) > 0)
+ *   u_accept       [sum gamma_b] fp32 uniforms in [0, 1), one per draft position
+ *   u_sample       [B] fp32 uniforms in [0, 1), for the correction or bonus draw
+ *   accept_len     [B] int32 out: drafts accepted
+ *   out_token      [B] int32 out: the correction token (accept_len < gamma_b) or the
+ *                  bonus token
+ * Decisions: accept when p(x) >= q(x) or when u * q(x), rounded to fp32, is < p(x).
+ * A draw is an inverse-CDF draw over masses quantised to 2^-40 and summed exactly as
+ * integers (threshold floor(floor(u * 2^24) * Z / 2^24)), so it does not depend on the
+ * order of the sums; an empty residual falls back to p.  A sequence with bad bounds, a
+ * token outside [0, V), q(x) = 0 or a uniform outside [0, 1) gets accept_len 0,
+ * out_token -1 and TVA_ERR_INVALID_ARG in *dev_status. */
+tva_status verify_chain_sampling(int batch, int vocab, int max_draft, long long p_rows, long long q_rows,
+                                 const int32_t* cu_draft, const float* p, const float* q,
+                                 const int32_t* draft_tok, const float* u_accept, const float* u_sample,
+                                 int32_t* accept_len, int32_t* out_token, int32_t* dev_status, void* stream);
+
 /* Description of the last host-side CUDA or driver failure seen by this thread
  * (the call that failed and its error string), "" if none.  Thread-local storage,
  * valid until the thread's next failing call. */

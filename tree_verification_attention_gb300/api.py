@@ -71,6 +71,8 @@ def load_library(path: str | None = None):
         "accept_longest_path": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "commit_accepted_kv": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_longlong, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _P]),
+        "verify_chain_sampling": (_I, [_I, _I, _I, ctypes.c_longlong, ctypes.c_longlong, _P, _P, _P, _P, _P, _P,
+                                       _P, _P, _P, _P]),
         "tva_status_string": (ctypes.c_char_p, [_I]),
         "tva_last_error": (ctypes.c_char_p, []),
     }
@@ -276,6 +278,39 @@ def commit_accepted_kv(cu_nodes, accept_len, accept_path, tree_k, tree_v, dst_ro
         _ptr(v_cache), _ptr(dev_status), _stream(stream))
     _check(code, "commit_accepted_kv")
     return dev_status
+
+
+def verify_chain_sampling(cu_draft, p, q, draft_tok, u_accept, u_sample, max_draft=None, accept_len=None,
+                          out_token=None, dev_status=None, stream=None):
+    """Modified rejection sampling over draft chains.  p [sum(gamma+1), V], q [sum gamma, V]
+    float32; draft_tok, u_accept [sum gamma]; u_sample [B]; cu_draft [B+1].
+    Returns (accept_len [B], out_token [B]) int32 CUDA tensors."""
+    for name, t in (("cu_draft", cu_draft), ("draft_tok", draft_tok)):
+        _dev(t, name, torch.int32)
+    for name, t in (("p", p), ("q", q), ("u_accept", u_accept), ("u_sample", u_sample)):
+        _dev(t, name, torch.float32)
+    B = cu_draft.numel() - 1
+    V = p.shape[1]
+    if q.shape[1] != V and q.numel() > 0:
+        raise ValueError("p and q must share the vocabulary")
+    if max_draft is None:
+        max_draft = int((cu_draft[1:] - cu_draft[:-1]).max().item()) if B > 0 else 0
+    dev = p.device
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_token is None:
+        out_token = torch.empty(B, dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # with no draft position at all, q / draft_tok / u_accept are never read: any
+    # valid address stands in for the empty tensors
+    some = lambda t: _ptr(t) if t.numel() > 0 else _ptr(p)  # noqa: E731
+    code = load_library().verify_chain_sampling(
+        B, V, int(max_draft), p.shape[0], q.shape[0] if q.numel() > 0 else 0, _ptr(cu_draft), _ptr(p), some(q),
+        some(draft_tok), some(u_accept), _ptr(u_sample), _ptr(accept_len), _ptr(out_token), _ptr(dev_status),
+        _stream(stream))
+    _check(code, "verify_chain_sampling")
+    return accept_len, out_token
 
 
 def tree_verify_attn_varlen_noalloc(q, k_cache, v_cache, tree_k, tree_v, parent, cu_prefix, cu_nodes,

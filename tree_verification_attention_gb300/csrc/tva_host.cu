@@ -383,4 +383,18 @@ tva_status commit_accepted_kv(int batch, int num_kv_heads, int head_dim, tva_dty
                                                                                             : TVA_ERR_CUDA;
 }
 
+tva_status verify_chain_sampling(int batch, int vocab, int max_draft, long long p_rows, long long q_rows,
+                                 const int32_t* cu_draft, const float* p, const float* q,
+                                 const int32_t* draft_tok, const float* u_accept, const float* u_sample,
+                                 int32_t* accept_len, int32_t* out_token, int32_t* dev_status, void* stream) {
+  if (batch < 1 || vocab < 1 || max_draft < 0 || p_rows < batch || q_rows < 0 || !cu_draft || !p || !q ||
+      !draft_tok || !u_accept || !u_sample || !accept_len || !out_token || !dev_status)
+    return TVA_ERR_INVALID_ARG;
+  tva::SamplingArgs a;
+  a.B = batch; a.V = vocab; a.max_draft = max_draft; a.p_rows = p_rows; a.q_rows = q_rows;
+  a.cu_draft = cu_draft; a.p = p; a.q = q; a.draft_tok = draft_tok; a.u_accept = u_accept;
+  a.u_sample = u_sample; a.accept_len = accept_len; a.out_token = out_token; a.status = dev_status;
+  return tva::launch_sampling(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -65,6 +65,20 @@ struct CommitArgs {
   int32_t* status;
 };
 
+struct SamplingArgs {
+  int B, V, max_draft;
+  long long p_rows, q_rows;
+  const int32_t* cu_draft;
+  const float* p;
+  const float* q;
+  const int32_t* draft_tok;
+  const float* u_accept;
+  const float* u_sample;
+  int32_t* accept_len;
+  int32_t* out_token;
+  int32_t* status;
+};
+
 // Records a host-side failure for tva_last_error() (thread-local).
 void record_error(const char* where, int code, const char* what);
 // Records `e` (if it is an error) and returns it unchanged.
@@ -97,5 +111,6 @@ cudaError_t launch_partials_tc(const PartialArgs& a, int W, int npt, cudaStream_
 cudaError_t launch_combine(const CombineArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
+cudaError_t launch_sampling(const SamplingArgs& a, cudaStream_t s);
 
 }  // namespace tva
