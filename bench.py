@@ -377,6 +377,28 @@ def main():
     committed_rows = int(alen.sum().item())
     commit_bytes = 2 * 2 * committed_rows * w.num_kv_heads * w.head_dim * (2 if w.dtype == "bf16" else 4)
 
+    # ---- stochastic chain verification (a "next" row, measured on its own): 8 chains of
+    # 8 drafts over a 128256-token vocabulary.
+    sp = [torch.from_numpy(x).to(dev) for x in workloads.make_chain_sampling_case(8, 8, 128256)]
+
+    def sample():
+        return api.verify_chain_sampling(sp[5], sp[0], sp[1], sp[2], sp[3], sp[4], max_draft=8, dev_status=status)
+
+    for _ in range(args.warmup):
+        sample()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda._sleep(int(20e6))
+    for i in range(K):
+        flush.fill_((i + 5) & 0xFF)
+        evs[i][0].record(stream)
+        s_alen, _ = sample()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    sample_ms = float(np.mean([evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]))
+    rows_read = int((2 - (s_alen == 8).int()).sum().item())   # residual: p and q rows; bonus: p row
+    sample_bytes = rows_read * 128256 * 4 + 8 * 8 * 16
+
     # ---- end to end through the public API from pinned host buffers
     pinned = {k: v.pin_memory() for k, v in host.items()}
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -486,6 +508,9 @@ def main():
         "kv_commit": {"us_per_launch": commit_ms * 1e3, "rows": committed_rows, "bytes": commit_bytes,
                       "gbs": commit_bytes / (commit_ms * 1e-3) / 1e9,
                       "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
+        "chain_sampling": {"workload": "B=8 chains, gamma=8, V=128256, fp32 p/q", "us_per_launch": sample_ms * 1e3,
+                           "bytes": sample_bytes, "gbs": sample_bytes / (sample_ms * 1e-3) / 1e9,
+                           "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }

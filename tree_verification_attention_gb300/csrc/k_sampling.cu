@@ -13,30 +13,32 @@
 // / 2^24), so the drawn token does not depend on the order of the sums.  An empty
 // residual (Z = 0) falls back to p.
 //
-// One CTA per sequence.  The draw reads the row once, coalesced: warp w sums the
-// quantised masses of its contiguous segment, a scan over the warp sums finds the
-// segment holding the threshold, and that warp alone rescans its segment 32 entries at
-// a time.
+// A sequence is served by a cluster of kCluster CTAs.  Every CTA repeats the cheap
+// acceptance tests (so all of them take the same decisions from the same inputs and
+// reach the cluster barriers together), then sums the quantised masses of its slice of
+// the vocabulary row with many loads in flight.  The slice sums are exchanged through
+// distributed shared memory; in the CTA whose slice holds the threshold an exclusive
+// scan of the per-thread chunk sums picks the chunk, and one thread walks it.
+#include <cooperative_groups.h>
+
 #include "tc_ptx.cuh"
 #include "tva_internal.h"
 
 namespace tva {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kCluster = 8;
+constexpr int kUnroll = 8;
 constexpr float kQScale = 1099511627776.0f;  // 2^40
 constexpr float kUScale = 16777216.0f;       // 2^24
 
 __device__ __forceinline__ unsigned long long quant(float w) {
   // w * 2^40 is exact (a power-of-two scale); truncation is the floor for w >= 0
   return __float2ull_rz(fmaxf(w, 0.f) * kQScale);
-}
-
-// mass of entry v of the row being drawn from
-__device__ __forceinline__ float mass(const float* prow, const float* qrow, int v) {
-  const float pv = __ldg(prow + v);
-  return qrow != nullptr ? fmaxf(0.f, __fsub_rn(pv, __ldg(qrow + v))) : pv;
 }
 
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
@@ -54,60 +56,38 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
   return x;
 }
 
-// Inverse-CDF draw over row entries [0, V) with uniform u (block-wide; every thread
-// calls it; returns the token in every thread, or -1 when the masses sum to zero).
-__device__ int draw(const float* prow, const float* qrow, int V, float u, unsigned long long* s_wsum,
-                    int* s_tok) {
+// Block-wide sum of two u64 values per thread (result in every thread).
+__device__ __forceinline__ void block_sum2(unsigned long long& a, unsigned long long& b,
+                                           unsigned long long* s) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int seg = (V + kWarps - 1) / kWarps;
-  const int v0 = min(V, warp * seg), v1 = min(V, v0 + seg);
-  unsigned long long s = 0;
-  for (int v = v0 + lane; v < v1; v += 32) s += quant(mass(prow, qrow, v));
-  s = warp_sum_u64(s);
-  if (lane == 0) s_wsum[warp] = s;
-  if (threadIdx.x == 0) *s_tok = -1;
+  a = warp_sum_u64(a);
+  b = warp_sum_u64(b);
+  if (lane == 0) { s[warp] = a; s[kWarps + warp] = b; }
   __syncthreads();
-  unsigned long long Z = 0, before = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) before += s_wsum[w];
-    Z += s_wsum[w];
-  }
-  if (Z > 0) {
-    const unsigned long long U = __float2ull_rz(u * kUScale);                 // < 2^24
-    const unsigned long long T = (__umul64hi(U, Z) << 40) | ((U * Z) >> 24);  // floor(U * Z / 2^24)
-    if (before <= T && T < before + s_wsum[warp]) {   // this warp's segment holds the draw
-      unsigned long long run = before;
-      for (int base = v0; base < v1; base += 32) {
-        const int v = base + lane;
-        const unsigned long long x = v < v1 ? quant(mass(prow, qrow, v)) : 0ull;
-        const unsigned long long incl = run + warp_incl_scan_u64(x, lane);
-        const unsigned hit = __ballot_sync(0xffffffffu, incl > T);
-        if (hit != 0u) {
-          if (lane == 0) *s_tok = base + __ffs(hit) - 1;
-          break;
-        }
-        run = __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
-  }
+  a = 0; b = 0;
+  for (int w = 0; w < kWarps; ++w) { a += s[w]; b += s[kWarps + w]; }
   __syncthreads();
-  const int tok = *s_tok;
-  __syncthreads();  // s_wsum / s_tok are reused by a second draw
-  return tok;
 }
 
+struct __align__(16) ClusterShared {
+  unsigned long long red[2 * kWarps];
+  unsigned long long slice[2];   // this CTA's residual and p sums (read by the cluster)
+  int first, tok;
+};
+
 __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
-  __shared__ unsigned long long s_wsum[kWarps];
-  __shared__ int s_first, s_tok;
+  __shared__ ClusterShared sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
-  const int b = blockIdx.x;
+  const int b = blockIdx.x / kCluster;
   const int g0 = __ldg(a.cu_draft + b);
   const int gamma = __ldg(a.cu_draft + b + 1) - g0;
   const float us = __ldg(a.u_sample + b);
   bool ok = g0 >= 0 && gamma >= 0 && gamma <= a.max_draft && (long long)g0 + gamma <= a.q_rows &&
             (long long)g0 + b + gamma + 1 <= a.p_rows && us >= 0.f && us < 1.f;
-  if (threadIdx.x == 0) s_first = gamma;
+  if (threadIdx.x == 0) sh.first = gamma;
   __syncthreads();
   for (int i = threadIdx.x; ok && i < gamma; i += kThreads) {
     const int x = __ldg(a.draft_tok + g0 + i);
@@ -116,34 +96,156 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
     const float px = __ldg(a.p + (size_t)(g0 + b + i) * a.V + x);
     const float qx = __ldg(a.q + (size_t)(g0 + i) * a.V + x);
     if (!(qx > 0.f)) { ok = false; break; }   // a draft token is drawn from q
-    if (!(px >= qx || __fmul_rn(u, qx) < px)) atomicMin(&s_first, i);
+    if (!(px >= qx || __fmul_rn(u, qx) < px)) atomicMin(&sh.first, i);
   }
+  // identical in every CTA of the cluster (same inputs), so all leave here together
   ok = __syncthreads_and(ok);
   if (!ok) {
-    if (threadIdx.x == 0) {
+    if (rank == 0 && threadIdx.x == 0) {
       set_status(a.status, kStatusInvalidArg);
       a.accept_len[b] = 0;
       a.out_token[b] = -1;
     }
     return;
   }
-  const int k = s_first;
+  const int k = sh.first;
   const float* prow = a.p + (size_t)(g0 + b + k) * a.V;
   const float* qrow = k < gamma ? a.q + (size_t)(g0 + k) * a.V : nullptr;
-  int tok = draw(prow, qrow, a.V, us, s_wsum, &s_tok);
-  if (tok < 0 && qrow != nullptr) tok = draw(prow, nullptr, a.V, us, s_wsum, &s_tok);
+
+  // ---- this CTA's slice, cut into contiguous per-thread chunks (multiples of 4 entries,
+  // read as 16-byte vectors when the rows are 16-byte aligned): chunk sums of the
+  // residual masses and of p
+  const int S = ((a.V + kCluster - 1) / kCluster + 3) & ~3;
+  const int v0 = min(a.V, rank * S), v1 = min(a.V, v0 + S);
+  const int C = ((v1 - v0 + kThreads - 1) / kThreads + 3) & ~3;
+  const int c0 = min(v1, v0 + (int)threadIdx.x * C), c1 = min(v1, c0 + C);
+  // every row starts on a 16-byte boundary
+  const bool vec = (a.V & 3) == 0 && ((reinterpret_cast<uintptr_t>(a.p) | reinterpret_cast<uintptr_t>(a.q)) & 15) == 0;
+  auto load4 = [&](const float* row, int v, float* out) {
+    if (vec && v + 3 < c1) {
+      const float4 t = __ldg(reinterpret_cast<const float4*>(row + v));
+      out[0] = t.x; out[1] = t.y; out[2] = t.z; out[3] = t.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) out[e] = v + e < c1 ? __ldg(row + v + e) : 0.f;
+    }
+  };
+  unsigned long long cr = 0, cp = 0;   // this thread's chunk sums
+  for (int base = c0; base < c1; base += 4 * kUnroll) {
+    float pv[kUnroll][4], qv[kUnroll][4];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int v = base + 4 * j;
+      if (v < c1) {
+        load4(prow, v, pv[j]);
+        if (qrow != nullptr) load4(qrow, v, qv[j]);
+        else qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
+      } else {
+        pv[j][0] = pv[j][1] = pv[j][2] = pv[j][3] = 0.f;
+        qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        cr += quant(fmaxf(0.f, __fsub_rn(pv[j][e], qv[j][e])));
+        cp += quant(pv[j][e]);
+      }
+  }
+  unsigned long long sr = cr, sp = cp;
+  block_sum2(sr, sp, sh.red);
+  if (threadIdx.x == 0) { sh.slice[0] = sr; sh.slice[1] = sp; }
+  cluster.sync();   // every slice sum is visible to the cluster
+
+  unsigned long long Zr = 0, Zp = 0, br = 0, bp = 0;
+  for (int r = 0; r < kCluster; ++r) {
+    const ClusterShared* peer = cluster.map_shared_rank(&sh, r);
+    const unsigned long long xr = peer->slice[0], xp = peer->slice[1];
+    if (r < rank) { br += xr; bp += xp; }
+    Zr += xr; Zp += xp;
+  }
+  cluster.sync();   // no CTA leaves (or reuses sh) while a peer may still read it
+
+  // residual when there is a rejection and its quantised mass is not empty, else p
+  const bool use_res = qrow != nullptr && Zr > 0;
+  const unsigned long long Z = use_res ? Zr : Zp, before = use_res ? br : bp;
+  const unsigned long long mine = use_res ? sr : sp;
+  if (Z == 0) {   // p itself is empty (all masses below 2^-40 or invalid)
+    if (rank == 0 && threadIdx.x == 0) {
+      set_status(a.status, kStatusInvalidArg);
+      a.accept_len[b] = k;
+      a.out_token[b] = -1;
+    }
+    return;
+  }
+  const unsigned long long U = __float2ull_rz(us * kUScale);                 // < 2^24
+  const unsigned long long T = (__umul64hi(U, Z) << 40) | ((U * Z) >> 24);  // floor(U * Z / 2^24)
+  if (!(before <= T && T < before + mine)) return;   // another CTA's slice holds the draw
+
+  // ---- the draw inside this slice: exclusive scan of the chunk sums, then the one
+  // chunk holding the threshold is read again and walked entry by entry
+  const unsigned long long cs = use_res ? cr : cp;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned long long incl = warp_incl_scan_u64(cs, lane);
+  if (lane == 31) sh.red[warp] = incl;
+  if (threadIdx.x == 0) sh.tok = -1;
+  __syncthreads();
+  unsigned long long woff = 0;
+  for (int w = 0; w < warp; ++w) woff += sh.red[w];
+  const unsigned long long excl = before + woff + incl - cs;   // running sum before this chunk
+  if (excl <= T && T < excl + cs) {
+    unsigned long long run = excl;
+    int tok = -1;
+    for (int base = c0; base < c1 && tok < 0; base += 4 * kUnroll) {
+      float pv[kUnroll][4], qv[kUnroll][4];
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int v = base + 4 * j;
+        if (v < c1) {
+          load4(prow, v, pv[j]);
+          if (use_res) load4(qrow, v, qv[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int v = base + 4 * j;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (tok < 0 && v + e < c1) {
+            run += use_res ? quant(fmaxf(0.f, __fsub_rn(pv[j][e], qv[j][e]))) : quant(pv[j][e]);
+            if (run > T) tok = v + e;
+          }
+        }
+      }
+    }
+    sh.tok = tok;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     a.accept_len[b] = k;
-    a.out_token[b] = tok;
-    if (tok < 0) set_status(a.status, kStatusInvalidArg);   // p itself sums to zero
+    a.out_token[b] = sh.tok;
   }
 }
 
 }  // namespace
 
 cudaError_t launch_sampling(const SamplingArgs& a, cudaStream_t s) {
-  return check_cuda(launch_pdl(sampling_kernel, dim3((unsigned)a.B), dim3(kThreads), 0, s, a),
-                    "launch sampling_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.B * kCluster);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return check_cuda(cudaLaunchKernelEx(&cfg, sampling_kernel, a), "launch sampling_kernel");
 }
 
 }  // namespace tva

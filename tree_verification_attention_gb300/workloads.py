@@ -321,3 +321,39 @@ def make_workload(config: int, seed: int | None = None, **overrides) -> Workload
         q=conv(q), k_cache=conv(k_cache), v_cache=conv(v_cache),
         tree_k=conv(tree_k), tree_v=conv(tree_v),
         softmax_scale=1.0 / math.sqrt(d), seed=seed, meta=meta)
+
+
+def make_chain_sampling_case(batch: int = 8, gamma: int = 8, vocab: int = 128256, seed: int = 2002,
+                             temperature: float = 3.0, overlap: float = 0.7):
+    """Synthetic inputs for stochastic chain verification: per sequence gamma draft
+    positions and gamma + 1 target positions over `vocab` tokens.
+
+    q rows are softmax(z * temperature) of N(0, 1) logits (peaked, like a drafter at
+    low temperature); the target rows at draft positions mix the draft row with an
+    independent one (``overlap`` of the mass shared), the bonus row is independent.
+    Draft tokens are drawn from their q rows; the uniforms are float32 in [0, 1).
+    Returns (p [B*(gamma+1), V], q [B*gamma, V], draft [B*gamma], u_accept [B*gamma],
+    u_sample [B], cu_draft [B+1]) as numpy arrays."""
+    rng = np.random.default_rng(seed)
+
+    def rows(n):
+        z = rng.standard_normal((n, vocab)).astype(np.float32) * temperature
+        z -= z.max(1, keepdims=True)
+        e = np.exp(z, dtype=np.float32)
+        return e / e.sum(1, keepdims=True, dtype=np.float32)
+
+    q = rows(batch * gamma)
+    p = rows(batch * (gamma + 1))
+    for b in range(batch):
+        for k in range(gamma):
+            r = b * (gamma + 1) + k
+            p[r] = overlap * q[b * gamma + k] + (1 - overlap) * p[r]
+    cdf = np.cumsum(q.astype(np.float64), 1)
+    cdf /= cdf[:, -1:]
+    draft = np.array([np.searchsorted(cdf[i], rng.random(), side="right") for i in range(batch * gamma)],
+                     dtype=np.int32)
+    draft = np.minimum(draft, vocab - 1)
+    u_accept = rng.random(batch * gamma).astype(np.float32)
+    u_sample = rng.random(batch).astype(np.float32)
+    cu_draft = np.arange(0, batch * gamma + 1, gamma, dtype=np.int32)
+    return p.astype(np.float32), q.astype(np.float32), draft, u_accept, u_sample, cu_draft
