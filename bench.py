@@ -33,9 +33,9 @@ METRIC = "tree-verify attn nodes/s & prefix-KV GB/s (1×GB300), fraction of roof
 
 
 def algorithmic_bytes(w):
-    """Bytes the method must move (bf16 storage): prefix K+V, tree K+V, Q, parent
+    """Bytes the method must move (16-bit or fp32 storage): prefix K+V, tree K+V, Q, parent
     (read by the partials kernel) and out + lse (written by the combine)."""
-    es = 2 if w.dtype == "bf16" else 4
+    es = 4 if w.dtype == "fp32" else 2
     d, Hq, Hkv, N = w.head_dim, w.num_q_heads, w.num_kv_heads, w.num_nodes
     prefix_kv = int(w.cu_prefix[-1]) * Hkv * d * es * 2
     k1 = prefix_kv + N * Hkv * d * es * 2 + N * Hq * d * es + 4 * N
@@ -253,6 +253,8 @@ def main():
         t = torch.from_numpy(np.ascontiguousarray(a))
         if w.dtype == "bf16":
             t = t.view(torch.int16).view(torch.bfloat16)
+        elif w.dtype == "fp16":
+            t = t.view(torch.int16).view(torch.float16)
         return t
 
     def i32(a):
@@ -375,7 +377,7 @@ def main():
     torch.cuda.synchronize()
     commit_ms = float(np.mean([evc[i][0].elapsed_time(evc[i][1]) for i in range(K)]))
     committed_rows = int(alen.sum().item())
-    commit_bytes = 2 * 2 * committed_rows * w.num_kv_heads * w.head_dim * (2 if w.dtype == "bf16" else 4)
+    commit_bytes = 2 * 2 * committed_rows * w.num_kv_heads * w.head_dim * (4 if w.dtype == "fp32" else 2)
 
     # ---- stochastic chain verification (a "next" row, measured on its own): 8 chains of
     # 8 drafts over a 128256-token vocabulary.

@@ -55,7 +55,9 @@ typedef enum {
 
 typedef enum {
   TVA_BF16 = 0, /* bfloat16 inputs and output, fp32 accumulation */
-  TVA_FP32 = 1  /* float32 inputs and output, fp32 accumulation  */
+  TVA_FP32 = 1, /* float32 inputs and output, fp32 accumulation  */
+  TVA_FP16 = 2  /* float16 inputs and output, fp32 accumulation (LongSpec's own
+                   precision, "Experiment details"); P is rounded to float16 */
 } tva_dtype;
 
 /* Problem description for the batched (varlen) entry points. */

@@ -9,7 +9,9 @@ import oracle
 from tree_verification_attention_gb300 import api
 
 # bf16: max-abs(out) <= 2e-2 and relative LSE error <= 1e-3; fp32: 1e-4 and 1e-5.
-TOL = {"bf16": (2e-2, 1e-3), "fp32": (1e-4, 1e-5)}
+# fp16 (10 mantissa bits against bf16's 7): P and out rounded to fp16 give relative
+# errors of a few 2^-11 on |out| <= ~4, so max-abs 5e-3; the LSE comes from fp32 sums.
+TOL = {"bf16": (2e-2, 1e-3), "fp32": (1e-4, 1e-5), "fp16": (5e-3, 5e-4)}
 
 
 def to_device(w):
@@ -19,6 +21,8 @@ def to_device(w):
         t = torch.from_numpy(np.ascontiguousarray(a))
         if w.dtype == "bf16":
             t = t.view(torch.int16).view(torch.bfloat16)
+        elif w.dtype == "fp16":
+            t = t.view(torch.int16).view(torch.float16)
         return t.to(dev)
 
     def i32(a):

@@ -24,6 +24,8 @@ SMALL = [
     (3, dict(prefix=1500)),
     (4, dict(prefix=(200, 1300))),
     (5, dict(prefix=900)),
+    (6, dict(prefix=1200)),
+    (6, dict(prefix=700, batch=3)),
 ]
 
 
@@ -48,6 +50,9 @@ EDGE = [
     # GQA groups that do not divide 128: M-tiles of 126 / 125 rows, padded in the partials
     dict(batch=2, Hq=12, Hkv=4, d=128, prefix=(77, 200), m=50, tree="random", dtype="bf16", vocab=8),
     dict(batch=1, Hq=10, Hkv=2, d=64, prefix=300, m=30, tree="random", dtype="fp32", vocab=8),
+    # float16 (LongSpec's precision): d = 64 and 128, a ragged batch, a full 128-node tree
+    dict(batch=3, Hq=8, Hkv=2, d=64, prefix=(0, 400), m=21, tree="random", dtype="fp16", vocab=8),
+    dict(batch=1, Hq=32, Hkv=8, d=128, prefix=300, m=128, tree="random", dtype="fp16", vocab=8),
 ]
 
 
@@ -116,7 +121,7 @@ def test_single_sequence_convenience_form():
     assert api.read_device_status() == 0
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5, 6])
 def test_full_size_sampled_rows(cfg):
     """Full-size workloads in the bench's launch configuration; the oracle evaluates
     a sample of rows one at a time."""
@@ -124,7 +129,7 @@ def test_full_size_sampled_rows(cfg):
     out, lse, st = _gpu.run_attention(w)
     assert st == 0
     rows = _gpu.sample_rows(w, 12, seed=cfg)
-    lazy = (lambda name: _LazyBf16(getattr(w, name))) if w.dtype == "bf16" else w.f64
+    lazy = (lambda name: _Lazy16(getattr(w, name), w.dtype)) if w.dtype != "fp32" else w.f64
     o_ref, l_ref = oracle.tree_verify_attention_rows(
         rows, w.f64("q"), lazy("k_cache"), lazy("v_cache"), w.cu_prefix, lazy("tree_k"),
         lazy("tree_v"), w.parent, w.cu_nodes, w.num_kv_heads, w.softmax_scale)
@@ -134,11 +139,12 @@ def test_full_size_sampled_rows(cfg):
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
 
 
-class _LazyBf16:
-    """Index-on-demand float64 view of bf16 bits (avoids a full float64 copy)."""
-    def __init__(self, bits):
+class _Lazy16:
+    """Index-on-demand float64 view of bf16 / fp16 bits (avoids a full float64 copy)."""
+    def __init__(self, bits, dtype):
         self.bits = bits
         self.shape = bits.shape
+        self.conv = workloads.bits_to_f64 if dtype == "bf16" else workloads.f16_bits_to_f64
 
     def __getitem__(self, idx):
-        return workloads.bits_to_f64(self.bits[idx])
+        return self.conv(self.bits[idx])

@@ -4,6 +4,7 @@ import pytest
 import torch
 
 from tree_verification_attention_gb300 import workloads as W
+from tree_verification_attention_gb300 import workloads
 
 
 def test_bf16_rounding_matches_torch():
@@ -84,3 +85,30 @@ def test_match_probability_and_sink_scaling():
     k = W.bits_to_f64(w5.k_cache)
     norms = np.linalg.norm(k[:, 0, :], axis=1)
     assert np.sum(norms > 2.5 * np.median(norms)) == 10     # 1% of 1000 keys boosted x4
+
+
+def test_beam_tree_levels_follow_the_widths():
+    """LongSpec's beam widths [4, 16, 16, 16, 16]: step s holds widths[s] nodes whose
+    parents are nodes of step s - 1, and a surviving candidate outscores every dropped one
+    (checked on the returned structure: level sizes and parent levels)."""
+    rng = np.random.default_rng(0)
+    for widths in ([4, 16, 16, 16, 16], [2, 3, 5], [1, 1, 1, 1], [7]):
+        par = workloads.beam_tree(rng, widths)
+        assert len(par) == sum(widths)
+        depth = workloads.tree_depths(par)
+        np.testing.assert_array_equal(np.bincount(depth)[1:], widths)
+        start = np.concatenate([[0], np.cumsum(widths)])
+        for lvl in range(1, len(widths)):
+            kids = par[start[lvl]:start[lvl + 1]]
+            assert ((kids >= start[lvl - 1]) & (kids < start[lvl])).all()
+
+
+def test_fp16_storage_is_ieee_half_rounding():
+    import torch
+    x = np.random.default_rng(1).standard_normal(10000).astype(np.float32) * 100
+    bits = workloads.f16_round_bits(x)
+    ref = torch.from_numpy(x).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(bits, ref)
+    np.testing.assert_array_equal(workloads.f16_bits_to_f64(bits), torch.from_numpy(x).to(torch.float16).double().numpy())
+    w = workloads.make_workload(6, prefix=64)
+    assert w.dtype == "fp16" and w.q.dtype == np.uint16 and w.num_nodes == 68

@@ -23,7 +23,7 @@ __all__ = [
 
 STATUS = {0: "TVA_OK", 1: "TVA_ERR_INVALID_ARG", 2: "TVA_ERR_UNSUPPORTED", 3: "TVA_ERR_BAD_TREE",
           4: "TVA_ERR_WORKSPACE", 5: "TVA_ERR_CUDA", 6: "TVA_ERR_TIMEOUT"}
-DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+DTYPES = {torch.bfloat16: 0, torch.float32: 1, torch.float16: 2}
 
 
 class TvaError(RuntimeError):

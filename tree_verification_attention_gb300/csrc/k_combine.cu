@@ -19,6 +19,10 @@
 // per launch from the expected number of partials per row group.  It is launched as a
 // programmatic dependent of the partials kernel: the walk that locates the row group
 // reads only the caller's cu_* arrays and runs before the wait for the partials.
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "tc_ptx.cuh"
 #include "tva_internal.h"
 
@@ -120,12 +124,22 @@ __global__ void __launch_bounds__(32 * WPB) combine_kernel(CombineArgs a) {
     for (int g = 0; g < CG; ++g)
       out[g] = make_float4(acc[g].x * inv, acc[g].y * inv, acc[g].z * inv, acc[g].w * inv);
   } else {
-    uint2* out = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + orow);
+    uint2* out = reinterpret_cast<uint2*>(static_cast<T*>(a.out) + orow);
 #pragma unroll
     for (int g = 0; g < CG; ++g) {
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[g].x * inv, acc[g].y * inv);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[g].z * inv, acc[g].w * inv);
-      out[g] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      uint32_t lo, hi;
+      if constexpr (std::is_same<T, __half>::value) {
+        const __half2 l = __floats2half2_rn(acc[g].x * inv, acc[g].y * inv);
+        const __half2 h = __floats2half2_rn(acc[g].z * inv, acc[g].w * inv);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __nv_bfloat162 l = __floats2bfloat162_rn(acc[g].x * inv, acc[g].y * inv);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[g].z * inv, acc[g].w * inv);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      out[g] = make_uint2(lo, hi);
     }
   }
   if (cs == 0) a.lse[(size_t)(R.s.n0 + node) * pr.Hq + head] = (Ms + log2f(den)) * 0.69314718055994530942f;
@@ -177,6 +191,7 @@ cudaError_t launch_dtype(const CombineArgs& a, cudaStream_t s) {
 
 cudaError_t launch_combine(const CombineArgs& a, int dtype, cudaStream_t s) {
   if (dtype == 1) return launch_dtype<float>(a, s);
+  if (dtype == 2) return launch_dtype<__half>(a, s);
   return launch_dtype<__nv_bfloat16>(a, s);
 }
 

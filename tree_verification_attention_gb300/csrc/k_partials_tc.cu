@@ -110,7 +110,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   mbar_wait(bar, parity, &never, kWaitNs);
 }
 
-template <int D>
+template <int D, bool kBF16>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     partials_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -247,8 +247,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false);
-      constexpr uint32_t idesc_o = idesc_bf16(128, D, true);
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, kBF16);
+      constexpr uint32_t idesc_o = idesc_bf16(128, D, true, kBF16);
       int ring = 0, sg = 0;
       uint32_t pbits = 0;  // bit w: parity of the next P_FULL[w] phase
       bool ok = true;
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                       x0, x1);
             const float p0 = ex2(x0), p1 = ex2(x1);
             lsx2 = f2_add(lsx2, f2_pack(p0, p1));
-            pk[c] = pack_bf16x2(p0, p1);
+            pk[c] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
           }
           tmem_st32(tl + s_col + 32 * h, pk);
         }
@@ -619,9 +619,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D bf16 map over [rows][heads][d] with a box of {64, box_heads, box_rows}.
-bool make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows, int box_heads,
-              int box_rows) {
+// 3-D 16-bit map over [rows][heads][d] with a box of {64, box_heads, box_rows}.
+bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int d, int heads, long long rows,
+              int box_heads, int box_rows) {
   auto fn = encode_fn();
   if (fn == nullptr) {
     record_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", 0, "entry point not found");
@@ -631,7 +631,7 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
   cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+  CUresult r = fn(m, type, 3, const_cast<void*>(base), dims, strides, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -641,29 +641,30 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows
   return true;
 }
 
-template <int D>
+template <int D, bool kBF16>
 cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s) {
+  constexpr CUtensorMapDataType type = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const Problem& pr = a.pr;
   CUtensorMap mq, mk, mv, mtk, mtv;
   const void* kbase = pr.kv_capacity > 0 ? a.k_cache : a.tree_k;
   const void* vbase = pr.kv_capacity > 0 ? a.v_cache : a.tree_v;
-  if (!make_map(&mq, a.q, D, pr.Hq, pr.node_capacity, pr.G, npt) ||
-      !make_map(&mk, kbase, D, pr.Hkv, pr.kv_capacity, 1, kKeyTile) ||
-      !make_map(&mv, vbase, D, pr.Hkv, pr.kv_capacity, 1, kKeyTile) ||
-      !make_map(&mtk, a.tree_k, D, pr.Hkv, pr.node_capacity, 1, kKeyTile) ||
-      !make_map(&mtv, a.tree_v, D, pr.Hkv, pr.node_capacity, 1, kKeyTile))
+  if (!make_map(&mq, type, a.q, D, pr.Hq, pr.node_capacity, pr.G, npt) ||
+      !make_map(&mk, type, kbase, D, pr.Hkv, pr.kv_capacity, 1, kKeyTile) ||
+      !make_map(&mv, type, vbase, D, pr.Hkv, pr.kv_capacity, 1, kKeyTile) ||
+      !make_map(&mtk, type, a.tree_k, D, pr.Hkv, pr.node_capacity, 1, kKeyTile) ||
+      !make_map(&mtv, type, a.tree_v, D, pr.Hkv, pr.node_capacity, 1, kKeyTile))
     return cudaErrorInvalidValue;
   constexpr int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = check_cuda(cudaFuncSetAttribute(partials_tc_kernel<D>,
+  cudaError_t e = check_cuda(cudaFuncSetAttribute(partials_tc_kernel<D, kBF16>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                              "cudaFuncSetAttribute(partials_tc_kernel)");
   if (e != cudaSuccess) return e;
   TcArgs ta{a, W, npt};
-  e = launch_pdl(partials_tc_kernel<D>, dim3(pr.U), dim3(kThreadsTc), (size_t)smem, s, mq, mk, mv, mtk,
+  e = launch_pdl(partials_tc_kernel<D, kBF16>, dim3(pr.U), dim3(kThreadsTc), (size_t)smem, s, mq, mk, mv, mtk,
                  mtv, ta);
   if (e != cudaSuccess) {
     cudaFuncAttributes fa{};
-    cudaFuncGetAttributes(&fa, partials_tc_kernel<D>);
+    cudaFuncGetAttributes(&fa, partials_tc_kernel<D, kBF16>);
     char what[160];
     snprintf(what, sizeof(what), "%s; kernel regs %d, max threads %d, smem %d+%d", cudaGetErrorString(e),
              fa.numRegs, fa.maxThreadsPerBlock, (int)fa.sharedSizeBytes, smem);
@@ -674,8 +675,9 @@ cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s
 
 }  // namespace
 
-cudaError_t launch_partials_tc(const PartialArgs& a, int W, int npt, cudaStream_t s) {
-  return a.pr.d == 64 ? launch_tc_typed<64>(a, W, npt, s) : launch_tc_typed<128>(a, W, npt, s);
+cudaError_t launch_partials_tc(const PartialArgs& a, bool bf16, int W, int npt, cudaStream_t s) {
+  if (bf16) return a.pr.d == 64 ? launch_tc_typed<64, true>(a, W, npt, s) : launch_tc_typed<128, true>(a, W, npt, s);
+  return a.pr.d == 64 ? launch_tc_typed<64, false>(a, W, npt, s) : launch_tc_typed<128, false>(a, W, npt, s);
 }
 
 }  // namespace tva

@@ -208,10 +208,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 
 // Instruction descriptor, kind::f16: BF16 A and B, FP32 accumulator, M x N.
 // b_mn_major: B stored with N contiguous (transposed) instead of K contiguous.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-  return (1u << 4)            // D format: F32
-         | (1u << 7)          // A format: BF16
-         | (1u << 10)         // B format: BF16
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major, bool bf16 = true) {
+  return (1u << 4)                   // D format: F32
+         | ((bf16 ? 1u : 0u) << 7)   // A format: BF16 (1) or F16 (0)
+         | ((bf16 ? 1u : 0u) << 10)  // B format: the same as A
          | ((b_mn_major ? 1u : 0u) << 16)
          | (static_cast<uint32_t>(N >> 3) << 17)
          | (static_cast<uint32_t>(M >> 4) << 24);
@@ -262,6 +262,11 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
 }
 

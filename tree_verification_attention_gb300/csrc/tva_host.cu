@@ -56,7 +56,7 @@ tva_status check_shape(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
   if (max_prefix < 0 || max_nodes < 1 || kv_cap < 0 || node_cap < 0) return TVA_ERR_INVALID_ARG;
   if (max_nodes > tva::kMaxNodes) return TVA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return TVA_ERR_UNSUPPORTED;
-  if (dtype != TVA_BF16 && dtype != TVA_FP32) return TVA_ERR_UNSUPPORTED;
+  if (dtype != TVA_BF16 && dtype != TVA_FP32 && dtype != TVA_FP16) return TVA_ERR_UNSUPPORTED;
   // index arithmetic inside the kernels is 32-bit for row counts
   if (kv_cap > (1LL << 31) - 1 - tva::kKeyTile || node_cap > (1LL << 24)) return TVA_ERR_INVALID_ARG;
   if ((long long)B * max_nodes > (1LL << 24) || (long long)B * max_prefix > (1LL << 40))
@@ -96,7 +96,7 @@ tva_status make_layout(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
   pr.single_nodes = single_nodes;
   pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.G = G; pr.d = d;
   pr.RG = W * npt * G;
-  pr.U = dtype == TVA_BF16 ? sms : sms * tva::simt_workers_per_sm();
+  pr.U = dtype == TVA_FP32 ? sms * tva::simt_workers_per_sm() : sms;  // the tensor-core kernels: one CTA per SM
   pr.max_prefix = max_prefix; pr.max_nodes = max_nodes;
   pr.kv_capacity = kv_cap; pr.node_capacity = node_cap;
   const long long groups = (long long)B * Hkv * ((max_nodes + W * npt - 1) / (W * npt));
@@ -133,8 +133,8 @@ tva_status run_partials(const Layout& L, int dtype, float softmax_scale, const v
   a.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + L.o_bytes);
   a.slots = L.slots;
   a.status = dev_status;
-  const cudaError_t e = dtype == TVA_BF16 ? tva::launch_partials_tc(a, L.W, L.npt, s)
-                                          : tva::launch_partials_simt(a, dtype, s);
+  const cudaError_t e = dtype == TVA_FP32 ? tva::launch_partials_simt(a, dtype, s)
+                                          : tva::launch_partials_tc(a, dtype == TVA_BF16, L.W, L.npt, s);
   return e == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
 }
 
@@ -355,13 +355,13 @@ tva_status commit_accepted_kv(int batch, int num_kv_heads, int head_dim, tva_dty
                               const void* tree_v, const int32_t* dst_row, void* k_cache, void* v_cache,
                               int32_t* dev_status, void* stream) {
   if (batch < 1 || num_kv_heads < 1 || (head_dim != 64 && head_dim != 128) ||
-      (dtype != TVA_BF16 && dtype != TVA_FP32) || node_capacity < 0 || max_nodes < 1 ||
+      (dtype != TVA_BF16 && dtype != TVA_FP32 && dtype != TVA_FP16) || node_capacity < 0 || max_nodes < 1 ||
       max_nodes > tva::kMaxNodes || kv_capacity < 0 || !cu_nodes || !accept_len || !accept_path || !tree_k ||
       !tree_v || !dst_row || !k_cache || !v_cache || !dev_status)
     return TVA_ERR_INVALID_ARG;
   if (!aligned16(tree_k) || !aligned16(tree_v) || !aligned16(k_cache) || !aligned16(v_cache))
     return TVA_ERR_INVALID_ARG;
-  const size_t row = (size_t)num_kv_heads * head_dim * (dtype == TVA_BF16 ? 2 : 4);
+  const size_t row = (size_t)num_kv_heads * head_dim * (dtype == TVA_FP32 ? 4 : 2);
   // The copy has no defined order, so no source row may alias a destination row; the
   // buffers are compared over their full extents.
   auto overlap = [](const void* x, size_t nx, const void* y, size_t ny) {

@@ -103,11 +103,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// dtype: 0 = bf16, 1 = fp32 (tva_dtype values)
+// dtype: 0 = bf16, 1 = fp32, 2 = fp16 (tva_dtype values)
 int simt_workers_per_sm();
 cudaError_t launch_partials_simt(const PartialArgs& a, int dtype, cudaStream_t s);
-// bf16, head_dim 64 or 128; W M-tiles of npt nodes per row group
-cudaError_t launch_partials_tc(const PartialArgs& a, int W, int npt, cudaStream_t s);
+// bf16 (bf16 = true) or fp16, head_dim 64 or 128; W M-tiles of npt nodes per row group
+cudaError_t launch_partials_tc(const PartialArgs& a, bool bf16, int W, int npt, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);

@@ -44,6 +44,9 @@ __all__ = [
     "chain_tree",
     "depth_limited_tree",
     "best_first_tree",
+    "beam_tree",
+    "f16_round_bits",
+    "f16_bits_to_f64",
     "tree_depths",
     "WORKLOAD_NAMES",
 ]
@@ -54,6 +57,7 @@ WORKLOAD_NAMES = {
     3: "bestfirst-bf16-P65536-m64-Hq32-Hkv8",
     4: "ragged-bf16-B8-P4096..32768-m32-Hq32-Hkv8",
     5: "sinks-bf16-P131072-m128-Hq64-Hkv8",
+    6: "beam-fp16-P32768-m68-Hq32-Hkv8",
 }
 
 
@@ -75,6 +79,16 @@ def bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def f16_round_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE float16 (nearest, ties to even); return the uint16 bits."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact float64 value of float16 values given as uint16 bits."""
+    return np.ascontiguousarray(bits).view(np.float16).astype(np.float64)
+
+
 # --------------------------------------------------------------------------- trees
 
 def random_tree(rng: np.random.Generator, m: int) -> np.ndarray:
@@ -88,6 +102,36 @@ def random_tree(rng: np.random.Generator, m: int) -> np.ndarray:
 def chain_tree(m: int) -> np.ndarray:
     """A linear draft of gamma = m tokens: parent[i] = i - 1."""
     return np.arange(-1, m - 1, dtype=np.int32)
+
+
+def beam_tree(rng: np.random.Generator, widths) -> np.ndarray:
+    """LongSpec's tree decoding shape ("Experiment details": dynamic beam search with
+    beam widths [4, 16, 16, 16, 16] per speculative step; low-likelihood branches stay in
+    the tree but are not expanded further).
+
+    Step 1 keeps the widths[0] best children of the prefix end.  Step s keeps the
+    widths[s] best of the candidates proposed by the previous step's nodes (each
+    proposes widths[s] children), scored by cumulative log-likelihood, a candidate
+    scoring its parent's score + log u, u ~ U(0, 1).  Nodes are numbered step by step
+    (topological).  A node none of whose candidates survives is a leaf.  Returns parent
+    ids (-1 for step-1 nodes), sum(widths) of them."""
+    widths = [int(w) for w in widths]
+    parent = [-1] * widths[0]
+    score = list(np.sort(np.log(rng.random(widths[0])))[::-1])
+    level = list(range(widths[0]))
+    for w in widths[1:]:
+        cand = []
+        for node in level:
+            for lu in np.log(rng.random(w)):
+                cand.append((score[node] + float(lu), node))
+        cand.sort(key=lambda c: -c[0])
+        new_level = []
+        for sc, par in cand[:w]:
+            parent.append(par)
+            score.append(sc)
+            new_level.append(len(parent) - 1)
+        level = new_level
+    return np.asarray(parent, dtype=np.int32)
 
 
 def tree_depths(parent: np.ndarray) -> np.ndarray:
@@ -200,12 +244,18 @@ class Workload:
     def f64(self, name: str) -> np.ndarray:
         """The exact float64 value of a floating-point input, as the kernels see it."""
         a = getattr(self, name)
-        return bits_to_f64(a) if self.dtype == "bf16" else a.astype(np.float64)
+        if self.dtype == "bf16":
+            return bits_to_f64(a)
+        if self.dtype == "fp16":
+            return f16_bits_to_f64(a)
+        return a.astype(np.float64)
 
 
 _DEFAULTS = {
     1: dict(batch=1, Hq=4, Hkv=1, d=64, prefix=256, m=8, tree="random", dtype="fp32",
             vocab=32),
+    6: dict(batch=1, Hq=32, Hkv=8, d=128, prefix=32768, m=68, tree="beam", widths=(4, 16, 16, 16, 16),
+            dtype="fp16", vocab=32000),
     2: dict(batch=1, Hq=32, Hkv=8, d=128, prefix=16384, m=8, tree="chain", dtype="bf16",
             vocab=32000, k_scale_half_heads=3.0),
     3: dict(batch=1, Hq=32, Hkv=8, d=128, prefix=65536, m=64, tree="best_first", width=4,
@@ -259,6 +309,11 @@ def make_workload(config: int, seed: int | None = None, **overrides) -> Workload
             parents.append(depth_limited_tree(rng, int(ms[b]), spec["max_depth"]))
         elif kind == "best_first":
             parents.append(best_first_tree(rng, int(ms[b]), spec["width"], spec["max_depth"]))
+        elif kind == "beam":
+            par = beam_tree(rng, spec["widths"])
+            if len(par) != int(ms[b]):
+                raise ValueError("a beam tree has sum(widths) nodes")
+            parents.append(par)
         elif kind == "given":
             parents.append(np.asarray(spec["parent"][b], dtype=np.int32))
         else:
@@ -310,6 +365,8 @@ def make_workload(config: int, seed: int | None = None, **overrides) -> Workload
         conv = bf16_round_bits
     elif dtype == "fp32":
         conv = lambda a: np.ascontiguousarray(a, dtype=np.float32)  # noqa: E731
+    elif dtype == "fp16":
+        conv = f16_round_bits
     else:
         raise ValueError(dtype)
     meta = {k: v for k, v in spec.items() if k not in ("parent",)}
