@@ -17,6 +17,7 @@ definition.
 * :mod:`oracle.expected_tokens` - expected tokens per verification cycle.
 * :mod:`oracle.kv_commit` - committing the accepted path's K/V into the cache.
 * :mod:`oracle.rejection_sampling` - stochastic verification of a draft chain.
+* :mod:`oracle.gdn_tree` - tree verification for Gated DeltaNet layers.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against facts fixed by the pages
 or by mathematics (closed forms, brute force, library routines on independently
@@ -28,6 +29,7 @@ from .acceptance import accept_longest_path
 from .expected_tokens import expected_tokens, survival_from_conditional, iid_expected_tokens
 from .kv_commit import commit_accepted_kv
 from .rejection_sampling import verify_chain_sampling, quantised_draw
+from .gdn_tree import gdn_tree_outputs, gdn_path_state
 
 __all__ = [
     "ancestor_mask",
@@ -42,4 +44,6 @@ __all__ = [
     "commit_accepted_kv",
     "verify_chain_sampling",
     "quantised_draw",
+    "gdn_tree_outputs",
+    "gdn_path_state",
 ]

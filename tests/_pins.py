@@ -438,3 +438,115 @@ def check_quantised_draw_against_searchsorted(draw_fn, rng, trials=300):
         if np.min(np.abs(c - t)) < 1e-6 * c[-1]:
             continue
         assert draw_fn(w, u) == int(np.searchsorted(c, t, side="right"))
+
+
+# ----------------------------------------------------------------------------- GDN trees
+def gdn_case(rng, B=2, H=2, d=6, max_m=9, beta_zero=False):
+    par = [np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, m)], np.int32)
+           for m in [int(rng.integers(1, max_m + 1)) for _ in range(B)]]
+    N = sum(len(p) for p in par)
+    unit = lambda x: x / np.linalg.norm(x, axis=-1, keepdims=True)  # noqa: E731
+    c = dict(q=unit(rng.standard_normal((N, H, d))), k=unit(rng.standard_normal((N, H, d))),
+             v=rng.standard_normal((N, H, d)), beta=rng.random((N, H)) if not beta_zero else np.zeros((N, H)),
+             alpha=0.5 + 0.5 * rng.random((N, H)), S0=rng.standard_normal((B, H, d, d)) * 0.3,
+             parent=np.concatenate(par).astype(np.int32),
+             cu_nodes=np.concatenate([[0], np.cumsum([len(p) for p in par])]).astype(np.int32))
+    return c
+
+
+def gdn_by_triangular_solve(c):
+    """The page's form: per sequence and head, with gamma_i the product of alpha over
+    node i's path, X_ij = beta_i (gamma_i / gamma_j) k_i . k_j for proper ancestors j,
+    (I + X) W = beta (V - Gamma K S0) solved by numpy.linalg.solve, and
+    o_i = gamma_i S0^T q_i + sum_{j anc-or-self of i} (gamma_i / gamma_j) (k_j . q_i) W_j."""
+    q, k, v, beta, alpha, S0 = (np.asarray(c[n], np.float64) for n in ("q", "k", "v", "beta", "alpha", "S0"))
+    N, H, _ = q.shape
+    out = np.zeros((N, H, v.shape[2]))
+    cu = c["cu_nodes"]
+    for b in range(len(cu) - 1):
+        n0, n1 = int(cu[b]), int(cu[b + 1])
+        m = n1 - n0
+        par = c["parent"][n0:n1]
+        anc = np.zeros((m, m), bool)        # anc[i, j]: j is i or an ancestor of i
+        for i in range(m):
+            j = i
+            while j >= 0:
+                anc[i, j] = True
+                j = int(par[j])
+        proper = anc & ~np.eye(m, dtype=bool)
+        for h in range(H):
+            a = alpha[n0:n1, h]
+            g = np.array([np.prod(a[anc[i]]) for i in range(m)])
+            K, Q, V, bt = k[n0:n1, h], q[n0:n1, h], v[n0:n1, h], beta[n0:n1, h]
+            ratio = g[:, None] / g[None, :]
+            X = np.where(proper, bt[:, None] * ratio * (K @ K.T), 0.0)
+            W = np.linalg.solve(np.eye(m) + X, bt[:, None] * (V - g[:, None] * (K @ S0[b, h])))
+            Y = np.where(anc, ratio * (Q @ K.T), 0.0)
+            out[n0:n1, h] = g[:, None] * (Q @ S0[b, h]) + Y @ W
+    return out
+
+
+def check_gdn_triangular_solve(fn, rng, trials=8):
+    for _ in range(trials):
+        c = gdn_case(rng)
+        np.testing.assert_allclose(fn(**c), gdn_by_triangular_solve(c), rtol=1e-10, atol=1e-10)
+
+
+def check_gdn_no_write(fn, rng):
+    """beta = 0: the state only decays, o_i = gamma_i S0^T q_i."""
+    c = gdn_case(rng, beta_zero=True)
+    out = fn(**c)
+    cu = c["cu_nodes"]
+    for b in range(len(cu) - 1):
+        n0, n1 = int(cu[b]), int(cu[b + 1])
+        for i in range(n1 - n0):
+            j, g = i, np.ones(c["q"].shape[1])
+            while j >= 0:
+                g = g * c["alpha"][n0 + j]
+                j = int(c["parent"][n0 + j])
+            for h in range(c["q"].shape[1]):
+                np.testing.assert_allclose(out[n0 + i, h], g[h] * (c["S0"][b, h].T @ c["q"][n0 + i, h]),
+                                           rtol=1e-12, atol=1e-12)
+
+
+def check_gdn_associative_recall(fn, rng, d=8, m=6):
+    """alpha = 1, beta = 1 and orthonormal keys: writing k_j stores v_j in place of
+    whatever S0 held at k_j, so reading with q = k_j returns v_j when j is on the
+    node's path (itself included) and S0^T k_j otherwise."""
+    par = np.array([-1, 0, 1, 0, 3, -1], np.int32)
+    Qm, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    K = Qm[:m]                                    # orthonormal rows
+    c = dict(k=K[:, None, :], v=rng.standard_normal((m, 1, d)), beta=np.ones((m, 1)), alpha=np.ones((m, 1)),
+             S0=rng.standard_normal((1, 1, d, d)), parent=par, cu_nodes=np.array([0, m], np.int32))
+    for target in range(m):
+        c["q"] = np.repeat(K[target][None, None, :], m, 0)
+        out = fn(**c)
+        for i in range(m):
+            j, on_path = i, False
+            while j >= 0:
+                on_path |= j == target
+                j = int(par[j])
+            expect = c["v"][target, 0] if on_path else c["S0"][0, 0].T @ K[target]
+            np.testing.assert_allclose(out[i, 0], expect, rtol=1e-10, atol=1e-10)
+
+
+def check_gdn_sibling_independence(fn, rng):
+    c = gdn_case(rng, B=1, max_m=9)
+    m = len(c["parent"])
+    if m < 3:
+        return
+    out = fn(**c)
+    j = int(rng.integers(1, m))
+    c2 = {n: np.array(x, copy=True) for n, x in c.items()}
+    c2["k"][j] = -c2["k"][j]
+    c2["v"][j] += 1.0
+    out2 = fn(**c2)
+    for i in range(m):
+        a, desc = i, False
+        while a >= 0:
+            desc |= a == j
+            a = int(c["parent"][a])
+        if not desc:
+            np.testing.assert_array_equal(out2[i], out[i])
+        else:
+            assert np.abs(out2[i] - out[i]).max() > 1e-9

@@ -281,3 +281,76 @@ def test_sampling_mutant_bonus_from_the_last_draft_position():
 
 def test_sampling_mutant_accepts_past_the_first_rejection():
     assert _sampling_pins_fail(_sampling_mutant(stop=False)) > 0
+
+
+# ----------------------------------------------------------------------------- GDN trees
+def _gdn_pins_fail(fn):
+    checks = [
+        lambda: _pins.check_gdn_triangular_solve(fn, np.random.default_rng(71), trials=3),
+        lambda: _pins.check_gdn_no_write(fn, np.random.default_rng(72)),
+        lambda: _pins.check_gdn_associative_recall(fn, np.random.default_rng(73)),
+        lambda: [_pins.check_gdn_sibling_independence(fn, np.random.default_rng(74 + s)) for s in range(3)],
+    ]
+    failed = 0
+    for c in checks:
+        try:
+            c()
+        except AssertionError:
+            failed += 1
+    return failed
+
+
+def _gdn_mutant(step, read_before=False, leaf_first=False):
+    """The oracle's per-path recurrence with the update `step` (S, k, v, beta, alpha -> S)
+    and optionally the read before the node's own write or the path reversed."""
+    def fn(q, k, v, beta, alpha, S0, parent, cu_nodes):
+        q = np.asarray(q, np.float64)
+        N, H, _ = q.shape
+        out = np.zeros((N, H, np.asarray(v).shape[2]))
+        for b in range(len(cu_nodes) - 1):
+            n0, n1 = int(cu_nodes[b]), int(cu_nodes[b + 1])
+            for i in range(n1 - n0):
+                path, j = [], i
+                while j >= 0:
+                    path.append(n0 + j)
+                    j = int(parent[n0 + j])
+                path = path if leaf_first else path[::-1]
+                for h in range(H):
+                    S = np.array(S0[b, h], np.float64)
+                    for t, node in enumerate(path):
+                        if read_before and node == n0 + i:
+                            break
+                        S = step(S, np.asarray(k[node, h], np.float64), np.asarray(v[node, h], np.float64),
+                                 beta[node, h], alpha[node, h])
+                    out[n0 + i, h] = S.T @ q[n0 + i, h]
+        return out
+    return fn
+
+
+_GDN_STEP = lambda S, k, v, b, a: a * (S - b * np.outer(k, k @ S)) + b * np.outer(k, v)  # noqa: E731
+
+
+def test_real_gdn_oracle_and_faithful_mutant_frame_pass():
+    from oracle import gdn_tree_outputs
+    assert _gdn_pins_fail(gdn_tree_outputs) == 0
+    assert _gdn_pins_fail(_gdn_mutant(_GDN_STEP)) == 0
+
+
+def test_gdn_mutant_decay_on_the_write():
+    assert _gdn_pins_fail(_gdn_mutant(lambda S, k, v, b, a: a * (S - b * np.outer(k, k @ S) + b * np.outer(k, v)))) > 0
+
+
+def test_gdn_mutant_read_before_write():
+    assert _gdn_pins_fail(_gdn_mutant(_GDN_STEP, read_before=True)) > 0
+
+
+def test_gdn_mutant_erase_without_beta():
+    assert _gdn_pins_fail(_gdn_mutant(lambda S, k, v, b, a: a * (S - np.outer(k, k @ S)) + b * np.outer(k, v))) > 0
+
+
+def test_gdn_mutant_leaf_first_path():
+    assert _gdn_pins_fail(_gdn_mutant(_GDN_STEP, leaf_first=True)) > 0
+
+
+def test_gdn_mutant_decay_ignored():
+    assert _gdn_pins_fail(_gdn_mutant(lambda S, k, v, b, a: S - b * np.outer(k, k @ S) + b * np.outer(k, v))) > 0

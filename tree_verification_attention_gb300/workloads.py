@@ -414,3 +414,46 @@ def make_chain_sampling_case(batch: int = 8, gamma: int = 8, vocab: int = 128256
     u_sample = rng.random(batch).astype(np.float32)
     cu_draft = np.arange(0, batch * gamma + 1, gamma, dtype=np.int32)
     return p.astype(np.float32), q.astype(np.float32), draft, u_accept, u_sample, cu_draft
+
+
+def make_gdn_case(batch: int = 1, heads: int = 32, d: int = 128, m: int = 64, tree: str = "best_first",
+                  seed: int = 3003, parents=None):
+    """Synthetic inputs for Gated DeltaNet tree verification (fp32 throughout).
+
+    q and k are L2-normalised per (node, head) as Gated DeltaNet layers normalise them;
+    v ~ N(0, 1); beta = sigmoid(z) in (0, 1); alpha = exp(-0.1 softplus(z)) (decays
+    near 1); the committed state S0 [B, H, d, d] is a sum of 32 random outer products
+    k v^T scaled by 1/4 (a state that has absorbed some context).  Trees: best-first
+    (width 4, depth <= 8), beam (LongSpec's widths), chain, or `parents` (a list of
+    parent arrays).  Returns a dict of numpy arrays."""
+    rng = np.random.default_rng(seed)
+    if parents is None:
+        parents = []
+        for _ in range(batch):
+            if tree == "best_first":
+                parents.append(best_first_tree(rng, m, 4, 8))
+            elif tree == "beam":
+                parents.append(beam_tree(rng, (4, 16, 16, 16, 16))[:m])
+            elif tree == "chain":
+                parents.append(chain_tree(m))
+            elif tree == "random":
+                parents.append(random_tree(rng, m))
+            else:
+                raise ValueError(tree)
+    sizes = [len(p) for p in parents]
+    cu_nodes = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    N = int(cu_nodes[-1])
+
+    def unit(x):
+        return (x / np.linalg.norm(x, axis=-1, keepdims=True)).astype(np.float32)
+
+    q = unit(rng.standard_normal((N, heads, d)))
+    k = unit(rng.standard_normal((N, heads, d)))
+    v = rng.standard_normal((N, heads, d)).astype(np.float32)
+    beta = (1 / (1 + np.exp(-rng.standard_normal((N, heads))))).astype(np.float32)
+    alpha = np.exp(-0.1 * np.log1p(np.exp(rng.standard_normal((N, heads))))).astype(np.float32)
+    ks = unit(rng.standard_normal((batch, heads, 32, d)))
+    vs = rng.standard_normal((batch, heads, 32, d)).astype(np.float32)
+    S0 = (0.25 * np.einsum("bhtk,bhtv->bhkv", ks, vs)).astype(np.float32)
+    parent = np.concatenate(parents).astype(np.int32) if parents else np.zeros(0, np.int32)
+    return dict(q=q, k=k, v=v, beta=beta, alpha=alpha, S0=S0, parent=parent, cu_nodes=cu_nodes)
