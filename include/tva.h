@@ -243,6 +243,27 @@ tva_status verify_chain_sampling(int batch, int vocab, int max_draft, long long 
                                  const int32_t* draft_tok, const float* u_accept, const float* u_sample,
                                  int32_t* accept_len, int32_t* out_token, int32_t* dev_status, void* stream);
 
+/* Tree verification for a Gated DeltaNet layer ("DFlash-TfM", Method 3, rollback-free
+ * tree verification for GDN): the state update S_t = alpha_t (I - beta_t k_t k_t^T)
+ * S_{t-1} + beta_t k_t v_t^T does not commute, so instead of an attention mask the tree
+ * (topologically ordered) becomes one unit-lower-triangular system over its ancestor
+ * pairs, solved by forward substitution, and the state itself is not updated (its
+ * commit waits for the accepted branch).  Node i's output is o_i = S_i^T q_i with S_i
+ * the state after running the update along the root-to-i path from S0.  The pages give
+ * no interface.  All pointers are device pointers, fp32, row-major:
+ *   batch, num_heads (H), head_dim (d: 64 or 128)
+ *   node_capacity rows of q, k, v, out [node_capacity, H, d] and beta, alpha [node_capacity, H]
+ *   max_nodes     bound on every m_b (<= 128)
+ *   cu_nodes      [B+1], parent [N] local ids in [-1, i) (as for the attention)
+ *   S0            [B, H, d, d] committed state at each sequence's prefix end (rows: keys)
+ *   out           [N, H, d]
+ * A sequence outside the bounds is skipped with TVA_ERR_INVALID_ARG, a non-topological
+ * parent array with TVA_ERR_BAD_TREE, in *dev_status. */
+tva_status gdn_tree_verify(int batch, int num_heads, int head_dim, int node_capacity, int max_nodes,
+                           const int32_t* cu_nodes, const int32_t* parent, const float* q, const float* k,
+                           const float* v, const float* beta, const float* alpha, const float* S0, float* out,
+                           int32_t* dev_status, void* stream);
+
 /* Description of the last host-side CUDA or driver failure seen by this thread
  * (the call that failed and its error string), "" if none.  Thread-local storage,
  * valid until the thread's next failing call. */

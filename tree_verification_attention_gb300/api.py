@@ -73,6 +73,7 @@ def load_library(path: str | None = None):
                                     _P, _P]),
         "verify_chain_sampling": (_I, [_I, _I, _I, ctypes.c_longlong, ctypes.c_longlong, _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P]),
+        "gdn_tree_verify": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "tva_status_string": (ctypes.c_char_p, [_I]),
         "tva_last_error": (ctypes.c_char_p, []),
     }
@@ -311,6 +312,29 @@ def verify_chain_sampling(cu_draft, p, q, draft_tok, u_accept, u_sample, max_dra
         _stream(stream))
     _check(code, "verify_chain_sampling")
     return accept_len, out_token
+
+
+def gdn_tree_verify(cu_nodes, parent, q, k, v, beta, alpha, S0, out=None, max_nodes=None, dev_status=None,
+                    stream=None):
+    """Gated DeltaNet tree verification.  q, k, v [N, H, d]; beta, alpha [N, H]; S0 [B, H, d, d];
+    all float32 CUDA tensors.  Returns out [N, H, d] float32."""
+    for name, t in (("cu_nodes", cu_nodes), ("parent", parent)):
+        _dev(t, name, torch.int32)
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("alpha", alpha), ("S0", S0)):
+        _dev(t, name, torch.float32)
+    B = cu_nodes.numel() - 1
+    N, H, d = q.shape
+    if max_nodes is None:
+        max_nodes = int((cu_nodes[1:] - cu_nodes[:-1]).max().item()) if B > 0 else 1
+    if out is None:
+        out = torch.empty_like(v)
+    if dev_status is None:
+        dev_status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    code = load_library().gdn_tree_verify(B, H, d, N, max(1, int(max_nodes)), _ptr(cu_nodes), _ptr(parent),
+                                          _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(S0),
+                                          _ptr(out), _ptr(dev_status), _stream(stream))
+    _check(code, "gdn_tree_verify")
+    return out
 
 
 def tree_verify_attn_varlen_noalloc(q, k_cache, v_cache, tree_k, tree_v, parent, cu_prefix, cu_nodes,

@@ -397,4 +397,19 @@ tva_status verify_chain_sampling(int batch, int vocab, int max_draft, long long 
   return tva::launch_sampling(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
 }
 
+tva_status gdn_tree_verify(int batch, int num_heads, int head_dim, int node_capacity, int max_nodes,
+                           const int32_t* cu_nodes, const int32_t* parent, const float* q, const float* k,
+                           const float* v, const float* beta, const float* alpha, const float* S0, float* out,
+                           int32_t* dev_status, void* stream) {
+  if (batch < 1 || num_heads < 1 || (head_dim != 64 && head_dim != 128) || node_capacity < 0 || max_nodes < 1 ||
+      max_nodes > tva::kMaxNodes || !cu_nodes || !parent || !q || !k || !v || !beta || !alpha || !S0 || !out ||
+      !dev_status)
+    return TVA_ERR_INVALID_ARG;
+  tva::GdnArgs a;
+  a.B = batch; a.H = num_heads; a.d = head_dim; a.max_nodes = max_nodes; a.node_capacity = node_capacity;
+  a.cu_nodes = cu_nodes; a.parent = parent; a.q = q; a.k = k; a.v = v; a.beta = beta; a.alpha = alpha;
+  a.S0 = S0; a.o = out; a.status = dev_status;
+  return tva::launch_gdn(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
+}
+
 }  // extern "C"

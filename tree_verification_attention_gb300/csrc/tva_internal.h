@@ -79,6 +79,20 @@ struct SamplingArgs {
   int32_t* status;
 };
 
+struct GdnArgs {
+  int B, H, d, max_nodes, node_capacity;
+  const int32_t* cu_nodes;
+  const int32_t* parent;
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* beta;
+  const float* alpha;
+  const float* S0;
+  float* o;
+  int32_t* status;
+};
+
 // Records a host-side failure for tva_last_error() (thread-local).
 void record_error(const char* where, int code, const char* what);
 // Records `e` (if it is an error) and returns it unchanged.
@@ -112,5 +126,6 @@ cudaError_t launch_combine(const CombineArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
 cudaError_t launch_sampling(const SamplingArgs& a, cudaStream_t s);
+cudaError_t launch_gdn(const GdnArgs& a, cudaStream_t s);
 
 }  // namespace tva
