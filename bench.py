@@ -401,6 +401,30 @@ def main():
     rows_read = int((2 - (s_alen == 8).int()).sum().item())   # residual: p and q rows; bonus: p row
     sample_bytes = rows_read * 128256 * 4 + 8 * 8 * 16
 
+    # ---- Gated DeltaNet tree verification (a "next" row, measured on its own): the same
+    # tree shape family, 32 heads of d = 128, fp32 state.
+    gc = workloads.make_gdn_case(batch=1, heads=32, d=128, m=64, tree="best_first")
+    gt = {n: torch.from_numpy(x).to(dev) for n, x in gc.items()}
+    g_out = torch.empty_like(gt["v"])
+
+    def gdn():
+        api.gdn_tree_verify(gt["cu_nodes"], gt["parent"], gt["q"], gt["k"], gt["v"], gt["beta"], gt["alpha"],
+                            gt["S0"], out=g_out, max_nodes=64, dev_status=status)
+
+    for _ in range(args.warmup):
+        gdn()
+    torch.cuda.synchronize()
+    evg = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    torch.cuda._sleep(int(20e6))
+    for i in range(K):
+        flush.fill_((i + 11) & 0xFF)
+        evg[i][0].record(stream)
+        gdn()
+        evg[i][1].record(stream)
+    torch.cuda.synchronize()
+    gdn_ms = float(np.mean([evg[i][0].elapsed_time(evg[i][1]) for i in range(K)]))
+    gdn_bytes = sum(x.nbytes for n, x in gc.items() if n not in ("parent", "cu_nodes")) + g_out.numel() * 4
+
     # ---- end to end through the public API from pinned host buffers
     pinned = {k: v.pin_memory() for k, v in host.items()}
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -513,6 +537,9 @@ def main():
         "chain_sampling": {"workload": "B=8 chains, gamma=8, V=128256, fp32 p/q", "us_per_launch": sample_ms * 1e3,
                            "bytes": sample_bytes, "gbs": sample_bytes / (sample_ms * 1e-3) / 1e9,
                            "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
+        "gdn_tree": {"workload": "B=1, H=32, d=128, 64-node best-first tree, fp32", "us_per_launch": gdn_ms * 1e3,
+                     "bytes": gdn_bytes, "gbs": gdn_bytes / (gdn_ms * 1e-3) / 1e9,
+                     "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }

@@ -257,7 +257,7 @@ tva_status verify_chain_sampling(int batch, int vocab, int max_draft, long long 
  *   cu_nodes      [B+1], parent [N] local ids in [-1, i) (as for the attention)
  *   S0            [B, H, d, d] committed state at each sequence's prefix end (rows: keys)
  *   out           [N, H, d]
- * A sequence outside the bounds is skipped with TVA_ERR_INVALID_ARG, a non-topological
+ * q, k, v, S0 and out are 16-byte aligned.  A sequence outside the bounds is skipped with TVA_ERR_INVALID_ARG, a non-topological
  * parent array with TVA_ERR_BAD_TREE, in *dev_status. */
 tva_status gdn_tree_verify(int batch, int num_heads, int head_dim, int node_capacity, int max_nodes,
                            const int32_t* cu_nodes, const int32_t* parent, const float* q, const float* k,

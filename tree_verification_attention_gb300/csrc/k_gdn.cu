@@ -17,8 +17,9 @@
 //   1. parents -> depth, per-node offsets into compact ancestor lists (thread 0; m <= 128);
 //      K staged in shared memory with padded rows;
 //   2. interaction values over ancestor pairs only: X (k.k) and Y (q.k), one pair per thread;
-//   3. K S_0 and Q S_0 for the thread's (rows, column) with S_0 read column-wise (coalesced);
-//      the right-hand side goes to shared memory, gamma_i Q S_0 stays in registers;
+//   3. K S_0 and Q S_0 for the thread's register tile (rows x 4 columns), with K and Q
+//      staged in shared memory and S_0 read as 16-byte vectors; the right-hand side goes
+//      to shared memory (over Q), gamma_i Q S_0 stays in registers;
 //   4. forward substitution one depth level at a time (nodes of a level are independent);
 //   5. the output sum over each node's ancestors-or-self.
 #include "tc_ptx.cuh"
@@ -30,24 +31,32 @@ namespace {
 constexpr int kThreadsGdn = 1024;
 constexpr int kMaxPairs = kMaxNodes * (kMaxNodes + 1) / 2;   // a chain of kMaxNodes
 
+constexpr int kCols = 32;   // output columns (of d_v) per CTA
+
 template <int D>
 struct GdnSmem {
   static constexpr int kKPitch = D + 1;                 // padded rows: distinct rows, distinct banks
+  static constexpr int kQPitch = D + 4;                 // padded, 16-byte aligned rows (Q, then W)
+  static constexpr int kWPitch = kCols + 4;
   static constexpr int kK = 0;                          // float [m][D+1]
-  static constexpr int kW = kK + kMaxNodes * kKPitch;   // float [m][D]
-  static constexpr int kX = kW + kMaxNodes * D;         // float [kMaxPairs] (proper-ancestor pairs)
+  static constexpr int kQ = kK + ((kMaxNodes * kKPitch + 3) & ~3);   // float [m][D+4], later W [m][kCols+4]
+  static constexpr int kS = kQ + kMaxNodes * kQPitch;   // float [D][kCols]: this CTA's columns of S_0
+  static constexpr int kX = kS + D * kCols;             // float [kMaxPairs] (proper-ancestor pairs)
   static constexpr int kY = kX + kMaxPairs;             // float [kMaxPairs] (ancestor-or-self pairs)
   static constexpr int kFloats = kY + kMaxPairs;
   static constexpr int kInts = 4 * kMaxNodes + 2 * (kMaxNodes + 2);   // par, dep, off, lvl, lvl0, fill
-  static constexpr size_t kBytes = (size_t)kFloats * 4 + (size_t)kInts * 4 + (size_t)kMaxNodes * 4;
+  static constexpr size_t kBytes = (size_t)kFloats * 4 + (size_t)kInts * 4 + (size_t)kMaxNodes * 4 * 3;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   using SM = GdnSmem<D>;
+  constexpr int CS = D / kCols;                // CTAs per (sequence, head)
   extern __shared__ float gsm[];
   float* sK = gsm + SM::kK;
-  float* sW = gsm + SM::kW;
+  float* sQ = gsm + SM::kQ;
+  float* sW = gsm + SM::kQ;                    // over Q once Q is no longer read
+  float* sS = gsm + SM::kS;
   float* sX = gsm + SM::kX;
   float* sY = gsm + SM::kY;
   int* s_par = reinterpret_cast<int*>(gsm + SM::kFloats);
@@ -57,26 +66,42 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   int* s_lvl0 = s_lvl + kMaxNodes;     // first index in s_lvl of each depth d (d <= m + 1)
   int* s_fill = s_lvl0 + kMaxNodes + 2;
   float* s_gam = reinterpret_cast<float*>(s_fill + kMaxNodes + 2);   // gamma_i
+  float* s_alpha = s_gam + kMaxNodes;
+  float* s_beta = s_alpha + kMaxNodes;
   __shared__ int s_ok, s_maxdep, s_pairs;
 
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
-  const int b = blockIdx.x / a.H, h = blockIdx.x % a.H;
+  const int cs = blockIdx.x % CS;
+  const int bh = blockIdx.x / CS;
+  const int b = bh / a.H, h = bh % a.H;
   const int n0 = __ldg(a.cu_nodes + b);
   const int m = __ldg(a.cu_nodes + b + 1) - n0;
   if (!(n0 >= 0 && m >= 0 && m <= a.max_nodes && (long long)n0 + m <= a.node_capacity)) {
-    if (threadIdx.x == 0) set_status(a.status, kStatusInvalidArg);
+    if (threadIdx.x == 0 && cs == 0) set_status(a.status, kStatusInvalidArg);
     return;
   }
   if (m == 0) return;
   const int tid = threadIdx.x;
   const size_t hs = (size_t)a.H * D;   // stride between nodes in q / k / v / o
+  const int c0 = cs * kCols;           // this CTA's first column of d_v
 
-  // ---- 1. tree bookkeeping and K
-  for (int i = tid; i < m; i += kThreadsGdn) s_par[i] = __ldg(a.parent + n0 + i);
+  // ---- 1. K, Q, this CTA's columns of S_0, the tree's scalars; bookkeeping by thread 0
+  for (int i = tid; i < m; i += kThreadsGdn) {
+    s_par[i] = __ldg(a.parent + n0 + i);
+    s_alpha[i] = __ldg(a.alpha + (size_t)(n0 + i) * a.H + h);
+    s_beta[i] = __ldg(a.beta + (size_t)(n0 + i) * a.H + h);
+  }
   for (int e = tid; e < m * D; e += kThreadsGdn) {
     const int i = e / D, r = e % D;
-    sK[i * SM::kKPitch + r] = __ldg(a.k + (size_t)(n0 + i) * hs + (size_t)h * D + r);
+    const size_t src = (size_t)(n0 + i) * hs + (size_t)h * D + r;
+    sK[i * SM::kKPitch + r] = __ldg(a.k + src);
+    sQ[i * SM::kQPitch + r] = __ldg(a.q + src);
+  }
+  const float* S0 = a.S0 + ((size_t)b * a.H + h) * D * D + c0;
+  for (int e = tid; e < D * (kCols / 4); e += kThreadsGdn) {
+    const int r = e / (kCols / 4), q4 = e % (kCols / 4);
+    *reinterpret_cast<float4*>(sS + r * kCols + 4 * q4) = __ldg(reinterpret_cast<const float4*>(S0 + (size_t)r * D) + q4);
   }
   __syncthreads();
   if (tid == 0) {
@@ -88,8 +113,7 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
       s_off[i] = off;
       off += s_dep[i];
       maxdep = max(maxdep, s_dep[i]);
-      const float al = __ldg(a.alpha + (size_t)(n0 + i) * a.H + h);
-      s_gam[i] = p < 0 ? al : al * s_gam[p];
+      s_gam[i] = p < 0 ? s_alpha[i] : s_alpha[i] * s_gam[p];
     }
     if (ok) {   // counting sort by depth (depths 1..maxdep <= m <= kMaxNodes)
       for (int d = 0; d <= maxdep + 1; ++d) s_lvl0[d] = 0;
@@ -106,7 +130,7 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   }
   __syncthreads();
   if (!s_ok) {
-    if (tid == 0) set_status(a.status, kStatusBadTree);
+    if (tid == 0 && cs == 0) set_status(a.status, kStatusBadTree);
     return;
   }
   const int pairs = s_pairs;
@@ -123,50 +147,57 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
     int j = i;
     float ratio = 1.f;               // gamma_i / gamma_j
     for (int t = 0; t < aidx; ++t) {
-      ratio *= __ldg(a.alpha + (size_t)(n0 + j) * a.H + h);
+      ratio *= s_alpha[j];
       j = s_par[j];
     }
     const float* kj = sK + j * SM::kKPitch;
     const float* ki = sK + i * SM::kKPitch;
-    const float* qi = a.q + (size_t)(n0 + i) * hs + (size_t)h * D;
+    const float* qi = sQ + i * SM::kQPitch;
     float kk = 0.f, qk = 0.f;
 #pragma unroll 8
     for (int r = 0; r < D; ++r) {
       kk = fmaf(ki[r], kj[r], kk);
-      qk = fmaf(__ldg(qi + r), kj[r], qk);
+      qk = fmaf(qi[r], kj[r], qk);
     }
-    const float beta_i = __ldg(a.beta + (size_t)(n0 + i) * a.H + h);
-    sX[pi] = aidx > 0 ? beta_i * ratio * kk : 0.f;
+    sX[pi] = aidx > 0 ? s_beta[i] * ratio * kk : 0.f;
     sY[pi] = ratio * qk;
   }
 
-  // ---- 3. K S_0 and Q S_0: thread -> column c, rows g, g + G, g + 2G, ...
-  constexpr int G = kThreadsGdn / D;          // row groups
-  constexpr int RPT = kMaxNodes / G;          // rows per thread (at most)
-  const int c = tid % D, g = tid / D;
-  float ks[RPT], qs[RPT];
+  // ---- 3. K S_0 and Q S_0 on this CTA's columns: thread -> 4 columns (cg) x rows rg, rg + RGS
+  constexpr int CG = kCols / 4;
+  constexpr int RGS = kThreadsGdn / CG;
+  constexpr int RPT = (kMaxNodes + RGS - 1) / RGS;
+  const int cg = tid % CG, rg = tid / CG;
+  float4 ks[RPT], qs[RPT];
 #pragma unroll
-  for (int t = 0; t < RPT; ++t) { ks[t] = 0.f; qs[t] = 0.f; }
-  const float* S0 = a.S0 + ((size_t)b * a.H + h) * D * D;
+  for (int t = 0; t < RPT; ++t) { ks[t] = make_float4(0.f, 0.f, 0.f, 0.f); qs[t] = ks[t]; }
+#pragma unroll 4
   for (int r = 0; r < D; ++r) {
-    const float s = __ldg(S0 + (size_t)r * D + c);
+    const float4 sv = *reinterpret_cast<const float4*>(sS + r * kCols + 4 * cg);
 #pragma unroll
     for (int t = 0; t < RPT; ++t) {
-      const int i = g + t * G;
+      const int i = rg + t * RGS;
       if (i < m) {
-        ks[t] = fmaf(sK[i * SM::kKPitch + r], s, ks[t]);
-        qs[t] = fmaf(__ldg(a.q + (size_t)(n0 + i) * hs + (size_t)h * D + r), s, qs[t]);
+        const float kv = sK[i * SM::kKPitch + r], qv = sQ[i * SM::kQPitch + r];
+        ks[t].x = fmaf(kv, sv.x, ks[t].x); ks[t].y = fmaf(kv, sv.y, ks[t].y);
+        ks[t].z = fmaf(kv, sv.z, ks[t].z); ks[t].w = fmaf(kv, sv.w, ks[t].w);
+        qs[t].x = fmaf(qv, sv.x, qs[t].x); qs[t].y = fmaf(qv, sv.y, qs[t].y);
+        qs[t].z = fmaf(qv, sv.z, qs[t].z); qs[t].w = fmaf(qv, sv.w, qs[t].w);
       }
     }
   }
+  __syncthreads();   // every read of Q is done: the buffer now takes the right-hand side
 #pragma unroll
   for (int t = 0; t < RPT; ++t) {
-    const int i = g + t * G;
+    const int i = rg + t * RGS;
     if (i < m) {
-      const size_t row = (size_t)(n0 + i) * hs + (size_t)h * D + c;
-      const float bt = __ldg(a.beta + (size_t)(n0 + i) * a.H + h);
-      sW[i * D + c] = bt * (__ldg(a.v + row) - s_gam[i] * ks[t]);   // right-hand side
-      qs[t] *= s_gam[i];
+      const float4 vv =
+          __ldg(reinterpret_cast<const float4*>(a.v + (size_t)(n0 + i) * hs + (size_t)h * D + c0) + cg);
+      const float bt = s_beta[i], gm = s_gam[i];
+      *reinterpret_cast<float4*>(sW + i * SM::kWPitch + 4 * cg) =
+          make_float4(bt * (vv.x - gm * ks[t].x), bt * (vv.y - gm * ks[t].y), bt * (vv.z - gm * ks[t].z),
+                      bt * (vv.w - gm * ks[t].w));
+      qs[t] = make_float4(gm * qs[t].x, gm * qs[t].y, gm * qs[t].z, gm * qs[t].w);
     }
   }
   __syncthreads();
@@ -175,15 +206,15 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   const int maxdep = s_maxdep;
   for (int d = 2; d <= maxdep; ++d) {
     const int l0 = s_lvl0[d], l1 = s_lvl0[d + 1];
-    for (int e = tid; e < (l1 - l0) * D; e += kThreadsGdn) {
-      const int i = s_lvl[l0 + e / D], cc = e % D;
-      float acc = sW[i * D + cc];
+    for (int e = tid; e < (l1 - l0) * kCols; e += kThreadsGdn) {
+      const int i = s_lvl[l0 + e / kCols], cc = e % kCols;
+      float acc = sW[i * SM::kWPitch + cc];
       int j = s_par[i];
       for (int t = 1; t < s_dep[i]; ++t) {      // proper ancestors, nearest first
-        acc = fmaf(-sX[s_off[i] + t], sW[j * D + cc], acc);
+        acc = fmaf(-sX[s_off[i] + t], sW[j * SM::kWPitch + cc], acc);
         j = s_par[j];
       }
-      sW[i * D + cc] = acc;
+      sW[i * SM::kWPitch + cc] = acc;
     }
     __syncthreads();
   }
@@ -191,15 +222,18 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   // ---- 5. outputs
 #pragma unroll
   for (int t = 0; t < RPT; ++t) {
-    const int i = g + t * G;
+    const int i = rg + t * RGS;
     if (i < m) {
-      float acc = qs[t];
+      float4 acc = qs[t];
       int j = i;
       for (int aa = 0; aa < s_dep[i]; ++aa) {   // ancestors-or-self, self first
-        acc = fmaf(sY[s_off[i] + aa], sW[j * D + c], acc);
+        const float y = sY[s_off[i] + aa];
+        const float4 w = *reinterpret_cast<const float4*>(sW + j * SM::kWPitch + 4 * cg);
+        acc.x = fmaf(y, w.x, acc.x); acc.y = fmaf(y, w.y, acc.y);
+        acc.z = fmaf(y, w.z, acc.z); acc.w = fmaf(y, w.w, acc.w);
         j = s_par[j];
       }
-      a.o[(size_t)(n0 + i) * hs + (size_t)h * D + c] = acc;
+      *(reinterpret_cast<float4*>(a.o + (size_t)(n0 + i) * hs + (size_t)h * D + c0) + cg) = acc;
     }
   }
 }
@@ -211,7 +245,8 @@ cudaError_t launch_gdn_typed(const GdnArgs& a, cudaStream_t s) {
                                                   (int)smem),
                              "cudaFuncSetAttribute(gdn_tree_kernel)");
   if (e != cudaSuccess) return e;
-  return check_cuda(launch_pdl(gdn_tree_kernel<D>, dim3((unsigned)(a.B * a.H)), dim3(kThreadsGdn), smem, s, a),
+  return check_cuda(launch_pdl(gdn_tree_kernel<D>, dim3((unsigned)(a.B * a.H * (D / kCols))), dim3(kThreadsGdn),
+                               smem, s, a),
                     "launch gdn_tree_kernel");
 }
 

@@ -405,6 +405,8 @@ tva_status gdn_tree_verify(int batch, int num_heads, int head_dim, int node_capa
       max_nodes > tva::kMaxNodes || !cu_nodes || !parent || !q || !k || !v || !beta || !alpha || !S0 || !out ||
       !dev_status)
     return TVA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S0) || !aligned16(out))
+    return TVA_ERR_INVALID_ARG;
   tva::GdnArgs a;
   a.B = batch; a.H = num_heads; a.d = head_dim; a.max_nodes = max_nodes; a.node_capacity = node_capacity;
   a.cu_nodes = cu_nodes; a.parent = parent; a.q = q; a.k = k; a.v = v; a.beta = beta; a.alpha = alpha;
