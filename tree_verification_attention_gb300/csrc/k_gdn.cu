@@ -14,8 +14,8 @@
 // The ratios gamma_i / gamma_j are products of alpha walked up from i to j (no division).
 //
 // One CTA (1024 threads) per (sequence, head), fp32 throughout:
-//   1. parents -> depth, per-node offsets into compact ancestor lists (thread 0; m <= 128);
-//      K staged in shared memory with padded rows;
+//   1. parents -> depth and path product (a thread per node), list offsets (a scan) and the
+//      depth-level order; K, Q and this CTA's columns of S_0 staged in shared memory;
 //   2. interaction values over ancestor pairs only: X (k.k) and Y (q.k), one pair per thread;
 //   3. K S_0 and Q S_0 for the thread's register tile (rows x 4 columns), with K and Q
 //      staged in shared memory and S_0 read as 16-byte vectors; the right-hand side goes
@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   float* s_gam = reinterpret_cast<float*>(s_fill + kMaxNodes + 2);   // gamma_i
   float* s_alpha = s_gam + kMaxNodes;
   float* s_beta = s_alpha + kMaxNodes;
-  __shared__ int s_ok, s_maxdep, s_pairs;
+  __shared__ int s_maxdep, s_pairs;
 
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   const size_t hs = (size_t)a.H * D;   // stride between nodes in q / k / v / o
   const int c0 = cs * kCols;           // this CTA's first column of d_v
 
-  // ---- 1. K, Q, this CTA's columns of S_0, the tree's scalars; bookkeeping by thread 0
+  // ---- 1. K, Q, this CTA's columns of S_0 and the tree's scalars; then the bookkeeping
   for (int i = tid; i < m; i += kThreadsGdn) {
     s_par[i] = __ldg(a.parent + n0 + i);
     s_alpha[i] = __ldg(a.alpha + (size_t)(n0 + i) * a.H + h);
@@ -103,36 +103,64 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
     const int r = e / (kCols / 4), q4 = e % (kCols / 4);
     *reinterpret_cast<float4*>(sS + r * kCols + 4 * q4) = __ldg(reinterpret_cast<const float4*>(S0 + (size_t)r * D) + q4);
   }
+  if (tid == 0) s_maxdep = 0;
+  for (int d = tid; d < kMaxNodes + 2; d += kThreadsGdn) s_lvl0[d] = 0;
   __syncthreads();
-  if (tid == 0) {
-    int ok = 1, off = 0, maxdep = 0;
-    for (int i = 0; i < m; ++i) {
-      const int p = s_par[i];
-      if (p < -1 || p >= i) { ok = 0; break; }
-      s_dep[i] = p < 0 ? 1 : s_dep[p] + 1;
-      s_off[i] = off;
-      off += s_dep[i];
-      maxdep = max(maxdep, s_dep[i]);
-      s_gam[i] = p < 0 ? s_alpha[i] : s_alpha[i] * s_gam[p];
+  // depth and gamma: one thread per node walks its own path (bounded: a parent id
+  // outside [-1, j) ends the walk; such a tree is rejected below)
+  bool ok = true;
+  if (tid < m) {
+    const int p0 = s_par[tid];
+    ok = p0 >= -1 && p0 < tid;
+    int j = tid, dep = 0;
+    float g = 1.f;
+    while (j >= 0 && dep < m) {
+      const int pj = s_par[j];
+      if (pj < -1 || pj >= j) break;
+      g *= s_alpha[j];
+      ++dep;
+      j = pj;
     }
-    if (ok) {   // counting sort by depth (depths 1..maxdep <= m <= kMaxNodes)
-      for (int d = 0; d <= maxdep + 1; ++d) s_lvl0[d] = 0;
-      for (int i = 0; i < m; ++i) s_lvl0[s_dep[i]]++;
-      int run = 0;
-      for (int d = 0; d <= maxdep; ++d) { const int c = s_lvl0[d]; s_lvl0[d] = run; run += c; }
-      s_lvl0[maxdep + 1] = run;
-      for (int d = 0; d <= maxdep; ++d) s_fill[d] = s_lvl0[d];
-      for (int i = 0; i < m; ++i) s_lvl[s_fill[s_dep[i]]++] = i;
-    }
-    s_ok = ok;
-    s_maxdep = maxdep;
-    s_pairs = off;
+    s_dep[tid] = dep;
+    s_gam[tid] = g;
+    atomicMax(&s_maxdep, dep);
+    atomicAdd(&s_lvl0[dep], 1);
   }
-  __syncthreads();
-  if (!s_ok) {
+  if (!__syncthreads_and(ok)) {
     if (tid == 0 && cs == 0) set_status(a.status, kStatusBadTree);
     return;
   }
+  // offsets of the ancestor-or-self lists: exclusive scan of the depths (m <= 128, four warps)
+  if (tid < kMaxNodes) {
+    const int lane = tid & 31, w = tid >> 5;
+    const int x = tid < m ? s_dep[tid] : 0;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_fill[w] = incl;   // warp totals (s_fill is reused below)
+    __syncwarp();
+    s_off[tid] = incl - x;              // within the warp; warp offsets added next
+  }
+  __syncthreads();
+  if (tid < kMaxNodes) {
+    int wo = 0;
+    for (int w = 0; w < (tid >> 5); ++w) wo += s_fill[w];
+    s_off[tid] += wo;
+    if (tid == m - 1) s_pairs = s_off[tid] + s_dep[tid];
+  }
+  __syncthreads();
+  // level order: counts are in s_lvl0; their exclusive prefix (depths 0..maxdep+1), then
+  // each node takes a slot of its level
+  if (tid == 0) {
+    int run = 0;
+    for (int d = 0; d <= s_maxdep + 1; ++d) { const int c = s_lvl0[d]; s_lvl0[d] = run; s_fill[d] = run; run += c; }
+  }
+  __syncthreads();
+  if (tid < m) s_lvl[atomicAdd(&s_fill[s_dep[tid]], 1)] = tid;
+  __syncthreads();
   const int pairs = s_pairs;
 
   // ---- 2. interaction values over ancestor pairs: pair index -> (node i, a-th entry of
