@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
     const long long seg_end = min(t_end, L.start + L.tiles);
     const int tile0 = L.tile;
     const int tile1 = (int)(seg_end - L.start);
-    const bool has_tree = tile1 == L.tiles;
+    const bool has_tree = tile0 == 0;   // the tree tile is a row group's first unit
     const SeqInfo s = L.s;
     const int slot = u + L.q;
     const bool slot_ok = slot < a.slots;  // cannot fail for a consistent layout
@@ -106,11 +106,11 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
       for (int k = 0; k < D / 8; ++k) o[k] = 0.f;
 
       for (int tile = tile0; tile < tile1; ++tile) {
-        const bool is_tree = tile == L.tiles - 1;
-        const int nkeys = is_tree ? s.m : min(kKeyTile, s.P - tile * kKeyTile);
+        const bool is_tree = tile == 0;
+        const int nkeys = is_tree ? s.m : min(kKeyTile, s.P - (tile - 1) * kKeyTile);
         const T* kb = static_cast<const T*>(is_tree ? a.tree_k : a.k_cache);
         const T* vb = static_cast<const T*>(is_tree ? a.tree_v : a.v_cache);
-        const size_t first = is_tree ? (size_t)s.n0 : (size_t)s.p0 + (size_t)tile * kKeyTile;
+        const size_t first = is_tree ? (size_t)s.n0 : (size_t)s.p0 + (size_t)(tile - 1) * kKeyTile;
         kb += first * kv_stride + (size_t)L.g * D;
         vb += first * kv_stride + (size_t)L.g * D;
         for (int k0 = 0; k0 < nkeys; k0 += kKT) {

@@ -217,9 +217,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           if (use > 0 && !mbar_wait(KV_EMPTY + 8 * stage, (use - 1) & 1, abort_flag, kWaitNs))
             return false;
           const int tile = S.tile0 + k;
-          const bool tree = tile == L.tiles - 1;
+          const bool tree = tile == 0;
           const CUtensorMap* m = tree ? (is_v ? &tm_tv : &tm_tk) : (is_v ? &tm_v : &tm_k);
-          const int z = tree ? L.s.n0 : L.s.p0 + tile * kKeyTile;
+          const int z = tree ? L.s.n0 : L.s.p0 + (tile - 1) * kKeyTile;
           mbar_expect_tx(KV_FULL + 8 * stage, C::kTileBytes);
           for (int h = 0; h < C::kHalves; ++h)
             tma_load_3d_hint(kv_s + stage * C::kTileBytes + h * kHalfBytes, m, 64 * h, L.g, z,
@@ -381,10 +381,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     while (ok && next_segment(pr, t, t_end, S)) {
       const Loc& L = S.L;
       const int n = S.n;
-      // The tree tile needs every parent id of the sequence.  Issue those loads now
-      // (one per thread) so their latency hides behind the prefix tiles; they are
-      // shared through shared memory when the tree tile comes.
-      const int my_parent = (S.tile0 + n == L.tiles && r < L.s.m) ? __ldg(a.parent + L.s.n0 + r) : 0;
+      // The tree tile (a row group's first unit) needs every parent id of the sequence:
+      // one load per thread, shared through shared memory when the tile's logits are in.
+      const int my_parent = (S.tile0 == 0 && r < L.s.m) ? __ldg(a.parent + L.s.n0 + r) : 0;
       const int mt = (W == 2) ? w : 0;
       const int node = (L.mp * W + mt) * npt + r / G;  // local node id of this row
       bool row_ok = r < npt * G && node < L.s.m;
@@ -393,12 +392,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       for (int i = 0; i < n_mine; ++i) {
         const int k = (W == 2) ? i : 2 * i + w;
         const int tile = S.tile0 + k;
-        const bool is_tree = tile == L.tiles - 1;
+        const bool is_tree = tile == 0;
         ok = __all_sync(0xffffffffu, mbar_wait(S_FULL + 8 * w, cnt & 1, abort_flag, kWaitNs));
         if (!ok) break;
         tc_fence_after();
         // keys of this tile: [0, lim) exist; the tree tile also needs the ancestor bit
-        const int lim = is_tree ? L.s.m : min(kKeyTile, L.s.P - tile * kKeyTile);
+        const int lim = is_tree ? L.s.m : min(kKeyTile, L.s.P - (tile - 1) * kKeyTile);
         if (is_tree || lim < kKeyTile) {
           // Rare tiles (the last, partial prefix tile; the tree tile): rewrite the logits
           // the row does not see to -inf in TMEM, 32 columns at a time, so the two

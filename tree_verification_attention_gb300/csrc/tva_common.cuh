@@ -5,9 +5,12 @@
 // Rows: for KV head g of sequence b, the m_b * G query rows (node i, query head
 // g*G + j) are numbered r = i*G + j and cut into row groups of RG = 128 * W rows.
 // Keys: each row group sees the P_b prefix keys, cut into tiles of 128, plus ONE more
-// tile holding the sequence's tree keys (masked to ancestors-and-self).
+// tile holding the sequence's tree keys (masked to ancestors-and-self), which comes
+// first: tile 0 is the tree tile and tile t >= 1 holds prefix keys [128 (t-1), 128 t).
+// (Its masking work then falls where a worker's pipeline is still filling instead of
+// at the end of the launch.)
 // A unit is one (row group, key tile) pair.  Units are numbered sequence by sequence,
-// KV head by KV head, row group by row group, tile by tile (the tree tile last).  The
+// KV head by KV head, row group by row group, tile by tile (the tree tile first).  The
 // U workers (CTAs) take equal contiguous ranges of c = ceil(T / U) units, so a
 // worker's range can cross row-group boundaries; each maximal piece of a range inside
 // one row group is a "segment" and produces one partial (O, LSE) per row.  The
