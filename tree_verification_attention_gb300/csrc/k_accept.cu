@@ -23,6 +23,20 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
   __shared__ int s_dep[kWarps][kMaxNodes];
   __shared__ int s_anc[kWarps][kMaxNodes];
   __shared__ int s_slot[kWarps][kMaxNodes + 1];
+  {
+    // Before waiting for the preceding kernel: pull this block's share of the input
+    // arrays into L2.  A prefetch is only a hint - no value is read here, and the loads
+    // after the wait see whatever the preceding kernels wrote - so it only shortens the
+    // dependent rounds of loads below.
+    const long long N = a.node_capacity;
+    const long long lo = N * blockIdx.x / gridDim.x, hi = N * (blockIdx.x + 1) / gridDim.x;
+    for (long long i = lo + (long long)threadIdx.x * 32; i < hi; i += (long long)blockDim.x * 32) {
+      ptx::prefetch_l2(a.parent + i);
+      ptx::prefetch_l2(a.draft_tok + i);
+      ptx::prefetch_l2(a.target_argmax + i + (long long)blockIdx.x * kWarps);
+    }
+    if (threadIdx.x == 0) ptx::prefetch_l2(a.cu_nodes + (long long)blockIdx.x * kWarps);
+  }
   ptx::pdl_wait();
   ptx::pdl_launch_dependents();
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
