@@ -64,10 +64,14 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+PARTIALS_SOURCES = ("k_partials_tc.cu", "tc_ptx.cuh", "tva_common.cuh", "tva_internal.h")
+
+
 def kernel_source_hash():
+    """Hash of the partials kernel's sources (the kernel whose DRAM traffic is recorded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tree_verification_attention_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in PARTIALS_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
