@@ -128,6 +128,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
 
+  if (warp == kProducerWarp && lane == 0) {  // kernel parameters: no dependence on earlier kernels
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_tk);
+    prefetch_tmap(&tm_tv);
+  }
   pdl_wait();  // launched as a programmatic dependent: inputs are final after this
   pdl_launch_dependents();
   stage_problem(a.pr, pr_s, reinterpret_cast<int*>(smem + C::kBarOff + C::kCuOff), C::kCuCap);
@@ -160,7 +167,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   float* m1_s = reinterpret_cast<float*>(smem + C::kBarOff + 512);  // [2][128]
   float* l1_s = m1_s + 256;                                         // [2][128]
 
-  if (threadIdx.x == 0) {
+  // The producer thread initialises the barriers and goes straight on to its first
+  // copies; the other warps wait for the initialisation (and the TMEM allocation) on
+  // named barrier 1, which the producer warp only arrives at.
+  uint32_t tmem = 0;
+  if (warp == kProducerWarp && lane == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(KV_FULL + 8 * s, 1);
       mbar_init(KV_EMPTY + 8 * s, 1);
@@ -179,24 +190,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     mbar_init(PAR_READY + 8, 128);
     *abort_flag = 0;
     fence_mbar_init();
+    __threadfence_block();
   }
-  if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+  if (warp == kProducerWarp) {
+    __syncwarp();
+    bar_arrive(1, kThreadsTc);
+  } else {
+    if (warp == kMmaWarp) {
+      tmem_alloc(smem_u32(tmem_slot), 512);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    bar_sync(1, kThreadsTc);
+    tc_fence_after();
+    tmem = *tmem_slot;
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_tk);
-      prefetch_tmap(&tm_tv);
       int ring = 0, sg = 0;
       bool ok = true;
       long long t = t_begin;
@@ -381,12 +393,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     while (ok && next_segment(pr, t, t_end, S)) {
       const Loc& L = S.L;
       const int n = S.n;
-      // The tree tile (a row group's first unit) needs every parent id of the sequence:
-      // one load per thread, shared through shared memory when the tile's logits are in.
-      const int my_parent = (S.tile0 == 0 && r < L.s.m) ? __ldg(a.parent + L.s.n0 + r) : 0;
       const int mt = (W == 2) ? w : 0;
       const int node = (L.mp * W + mt) * npt + r / G;  // local node id of this row
       bool row_ok = r < npt * G && node < L.s.m;
+      // The tree tile (a row group's first unit, taken by stream 0 when W = 1) needs the
+      // row's ancestor bits.  They depend only on the parent ids, so they are found here,
+      // while the first K tile is still on its way: one parent load per thread, shared
+      // through shared memory, then the walk up from the row's node.
+      uint32_t anc[4] = {0u, 0u, 0u, 0u};
+      if (S.tile0 == 0 && (W == 2 || w == 0)) {
+        int* ps = par_s + w * 128;
+        if (r < L.s.m) ps[r] = __ldg(a.parent + L.s.n0 + r);
+        mbar_arrive(PAR_READY + 8 * w);
+        ok = __all_sync(0xffffffffu, mbar_wait(PAR_READY + 8 * w, trees & 1, abort_flag, kWaitNs));
+        ++trees;
+        if (!ok) break;
+        if (row_ok && !ancestor_bits_shared(ps, node, anc)) set_status(a.status, kStatusBadTree);
+      }
       const int n_mine = (W == 2) ? n : (n - w + 1) / 2;
       float m_run = -INFINITY, l_run = 0.f;
       for (int i = 0; i < n_mine; ++i) {
@@ -402,17 +425,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           // Rare tiles (the last, partial prefix tile; the tree tile): rewrite the logits
           // the row does not see to -inf in TMEM, 32 columns at a time, so the two
           // passes below carry no masking code.
-          uint32_t anc[4] = {0u, 0u, 0u, 0u};
-          if (is_tree) {
-            // the segment's parent ids, loaded at its start, meet in shared memory
-            int* ps = par_s + w * 128;
-            if (r < L.s.m) ps[r] = my_parent;
-            mbar_arrive(PAR_READY + 8 * w);
-            ok = __all_sync(0xffffffffu, mbar_wait(PAR_READY + 8 * w, trees & 1, abort_flag, kWaitNs));
-            ++trees;
-            if (!ok) break;
-            if (row_ok && !ancestor_bits_shared(ps, node, anc)) set_status(a.status, kStatusBadTree);
-          }
 #pragma unroll 1
           for (int ck = 0; ck < 4; ++ck) {
             uint32_t sv[32];
