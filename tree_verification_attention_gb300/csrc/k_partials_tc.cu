@@ -8,8 +8,10 @@
 // one more 128-key tile whose logits are masked with the row's ancestor bits.
 //
 // How (one CTA per SM, 320 threads):
-//   warp 8  (producer): TMA loads of Q (once per segment) and of the K / V tiles into
-//           a ring of shared-memory stages, 128-byte swizzled.
+//   warp 8  (producer): TMA loads of Q (once per segment; with one M-tile per row group
+//           into two alternating buffers, so a worker's next segment does not wait for
+//           the current one's Q to be released) and of the K / V tiles into a ring of
+//           shared-memory stages, 128-byte swizzled.
 //   warp 9  (MMA):      single-thread tcgen05.mma issue.  S = Q K^T (both operands in
 //           shared memory) into TMEM; O += P V with P read from TMEM (P overwrites
 //           the first half of its S buffer as packed bf16) and V from shared memory.
@@ -104,6 +106,13 @@ __device__ __forceinline__ bool ancestor_bits_shared(const int* par, int i, uint
   return true;
 }
 
+// Q buffers: with one M-tile per row group (W = 1) the Q region holds two M-tiles, so
+// segments alternate between two buffers and the next segment's Q is loaded while the
+// current one is still in use; with W = 2 one buffer holds both M-tiles.
+__device__ __forceinline__ int q_buffer(int W, int sg) { return W == 1 ? (sg & 1) : 0; }
+// Earlier segments that used the same buffer.
+__device__ __forceinline__ int q_use(int W, int sg) { return W == 1 ? (sg >> 1) : sg; }
+
 // Waits that ignore the abort flag (used only while draining).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   volatile int never = 0;
@@ -151,16 +160,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   const uint32_t bar0 = sbase + C::kBarOff;
   const uint32_t KV_FULL = bar0;                        // [kStages]
   const uint32_t KV_EMPTY = bar0 + 8 * C::kStages;      // [kStages]
-  const uint32_t Q_FULL = bar0 + 16 * C::kStages;
-  const uint32_t Q_EMPTY = Q_FULL + 8;
-  const uint32_t S_FULL = Q_EMPTY + 8;                  // [2]
+  const uint32_t Q_FULL = bar0 + 16 * C::kStages;      // [2]
+  const uint32_t Q_EMPTY = Q_FULL + 16;                 // [2]
+  const uint32_t S_FULL = Q_EMPTY + 16;                 // [2]
   const uint32_t P_FULL = S_FULL + 16;                  // [2]
   const uint32_t O_FULL = P_FULL + 16;                  // [2]
   const uint32_t O_FREE = O_FULL + 16;
   const uint32_t M1_READY = O_FREE + 8;
   const uint32_t DRAIN = M1_READY + 8;
   const uint32_t PAR_READY = DRAIN + 8;                 // [2]
-  uint8_t* misc = smem + C::kBarOff + 16 * C::kStages + 8 * 14;
+  uint8_t* misc = smem + C::kBarOff + 16 * C::kStages + 8 * 16;
   int* par_s = reinterpret_cast<int*>(smem + C::kBarOff + 2560);   // [2][128] parent ids
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
@@ -176,8 +185,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       mbar_init(KV_FULL + 8 * s, 1);
       mbar_init(KV_EMPTY + 8 * s, 1);
     }
-    mbar_init(Q_FULL, 1);
-    mbar_init(Q_EMPTY, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(Q_FULL + 8 * b, 1);
+      mbar_init(Q_EMPTY + 8 * b, 1);
+    }
     for (int w = 0; w < 2; ++w) {
       mbar_init(S_FULL + 8 * w, 1);
       mbar_init(P_FULL + 8 * w, 128);
@@ -217,12 +228,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint64_t evict_first = policy_evict_first();  // K/V are read once
       while (ok && next_segment(pr, t, t_end, S)) {
         const Loc& L = S.L;
-        if (sg > 0 && !mbar_wait(Q_EMPTY, (sg - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-        mbar_expect_tx(Q_FULL, (uint32_t)W * C::kHalves * q_box_bytes);
+        const int qb = q_buffer(W, sg), quse = q_use(W, sg);
+        if (quse > 0 && !mbar_wait(Q_EMPTY + 8 * qb, (quse - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        mbar_expect_tx(Q_FULL + 8 * qb, (uint32_t)W * C::kHalves * q_box_bytes);
         for (int mt = 0; mt < W; ++mt)
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(q_s + (mt * C::kHalves + h) * kHalfBytes, &tm_q, 64 * h, L.g * G,
-                        L.s.n0 + (L.mp * W + mt) * npt, Q_FULL);
+            tma_load_3d(q_s + ((qb + mt) * C::kHalves + h) * kHalfBytes, &tm_q, 64 * h, L.g * G,
+                        L.s.n0 + (L.mp * W + mt) * npt, Q_FULL + 8 * qb);
         const int n = S.n;
         auto load = [&](int k, bool is_v) -> bool {
           const int stage = ring % C::kStages, use = ring / C::kStages;
@@ -254,7 +266,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // drain: every copy this thread started has landed before TMEM / smem go away
       for (int i = max(0, ring - C::kStages); i < ring; ++i)
         drain_wait(KV_FULL + 8 * (i % C::kStages), (i / C::kStages) & 1);
-      if (sg > 0) drain_wait(Q_FULL, (sg - 1) & 1);
+      for (int b = 0; b < 2; ++b) {  // the last load into each Q buffer
+        const int uses = (W == 1) ? (sg + 1 - b) / 2 : (b == 0 ? sg : 0);
+        if (uses > 0) drain_wait(Q_FULL + 8 * b, (uses - 1) & 1);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
@@ -280,9 +295,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const uint32_t k_lo = (uint32_t)sdesc_sw128(kv_s, 16, 1024);
       const uint32_t v_lo = (uint32_t)sdesc_sw128(kv_s, kHalfBytes, 1024);
       const uint32_t q_lo = (uint32_t)sdesc_sw128(q_s, 16, 1024);
+      int qb = 0;  // Q buffer of the current segment
       auto issue_s = [&](int w, int mt, int idx) {
         const uint32_t kl = k_lo + (uint32_t)((idx % C::kStages) * C::kTileBytes >> 4);
-        const uint32_t ql = q_lo + (uint32_t)(mt * C::kHalves * kHalfBytes >> 4);
+        const uint32_t ql = q_lo + (uint32_t)((qb + mt) * C::kHalves * kHalfBytes >> 4);
         const uint32_t dt = tmem + w * 128;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -312,7 +328,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       };
       while (ok && next_segment(pr, t, t_end, S)) {
         const int n = S.n;
-        if (!mbar_wait(Q_FULL, sg & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        qb = q_buffer(W, sg);
+        if (!mbar_wait(Q_FULL + 8 * qb, q_use(W, sg) & 1, abort_flag, kWaitNs)) { ok = false; break; }
         tc_fence_after();
         if (W == 2) {
           // ring: K_k at ring + 2k, V_k at ring + 2k + 1
@@ -320,7 +337,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           issue_s(0, 0, ring);
           issue_s(1, 1, ring);
           tc_commit(KV_EMPTY + 8 * (ring % C::kStages));
-          if (n == 1) tc_commit(Q_EMPTY);
+          if (n == 1) tc_commit(Q_EMPTY + 8 * qb);
           for (int k = 0; k < n && ok; ++k) {
             const int vi = ring + 2 * k + 1, ki = ring + 2 * k + 2;
             if (!(ok = wait_kv(vi))) break;
@@ -336,7 +353,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 issue_s(w, w, ki);
                 if (w == 1) {
                   tc_commit(KV_EMPTY + 8 * (ki % C::kStages));
-                  if (k + 1 == n - 1) tc_commit(Q_EMPTY);
+                  if (k + 1 == n - 1) tc_commit(Q_EMPTY + 8 * qb);
                 }
               }
             }
@@ -353,7 +370,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             issue_s(1, 0, rK(1));
             tc_commit(KV_EMPTY + 8 * (rK(1) % C::kStages));
           }
-          if (n <= 2) tc_commit(Q_EMPTY);
+          if (n <= 2) tc_commit(Q_EMPTY + 8 * qb);
           for (int j = 0; j < n && ok; ++j) {
             const int w = j & 1;
             if (!(ok = wait_kv(rV(j)))) break;
@@ -367,7 +384,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
               if (!(ok = wait_kv(rK(j + 2)))) break;
               issue_s(w, 0, rK(j + 2));
               tc_commit(KV_EMPTY + 8 * (rK(j + 2) % C::kStages));
-              if (j + 2 == n - 1) tc_commit(Q_EMPTY);
+              if (j + 2 == n - 1) tc_commit(Q_EMPTY + 8 * qb);
             }
           }
         }
