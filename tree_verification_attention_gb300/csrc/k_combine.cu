@@ -21,6 +21,7 @@
 // reads only the caller's cu_* arrays and runs before the wait for the partials.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "tc_ptx.cuh"
@@ -41,7 +42,9 @@ __global__ void __launch_bounds__(32 * WPB) combine_kernel(CombineArgs a) {
   const int MT = mtile_rows(pr.G);
   const int W = pr.RG / MT;
   const int RGP = W * 128;
-  const long long wid = (long long)blockIdx.x * WPB + (threadIdx.x >> 5);
+  // Work items are dealt to the blocks round-robin (item = warp * blocks + block), so
+  // that every SM ends up with the same number of items to within one per block.
+  const long long wid = (long long)(threadIdx.x >> 5) * gridDim.x + blockIdx.x;
   const long long per_group = (long long)(RGP / 32) * NCG;
   const long long qg = wid / per_group;
   const int rb = (int)(wid % per_group) / NCG;  // 32-row block
@@ -150,13 +153,35 @@ long long max_row_groups(const Problem& pr) {
   return (long long)pr.B * pr.Hkv * (((long long)pr.max_nodes * pr.G + pr.RG - 1) / pr.RG);
 }
 
-// WPB warps per block: as many as keep the registers of two blocks per SM or more.
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 1;
+    n = v > 0 ? v : 1;
+  }
+  return n;
+}
+
+// WPB warps per block: as many as keep the registers of two blocks per SM or more.  One
+// item per warp; when the items fill less than one wave of blocks, the grid is widened
+// to a full wave (never past one block per item) and the round-robin deal spreads the
+// items evenly over it.
 template <typename T, int D, int CG, int NB>
 cudaError_t launch_typed(const CombineArgs& a, cudaStream_t s) {
   constexpr int WPB = CG == 1 ? 8 : 4;
   const int RGP = padded_group_rows(a.pr.RG, a.pr.G);
   const long long warps = max_row_groups(a.pr) * (RGP / 32) * (D / 4 / CG);
-  const long long blocks = (warps + WPB - 1) / WPB;
+  static int per_sm = 0;
+  if (per_sm == 0 &&
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<T, D, CG, NB, WPB>, 32 * WPB, 0) !=
+           cudaSuccess ||
+       per_sm < 1))
+    per_sm = 1;
+  const long long wave = (long long)sm_count() * per_sm;
+  long long blocks = (warps + WPB - 1) / WPB;
+  if (blocks < wave) blocks = std::min<long long>(wave, warps);
   if (blocks <= 0) return cudaSuccess;
   return check_cuda(launch_pdl(combine_kernel<T, D, CG, NB, WPB>, dim3((unsigned)blocks), dim3(32 * WPB), 0,
                                s, a),
