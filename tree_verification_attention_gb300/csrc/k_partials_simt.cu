@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
   float* ps = vs + kKT * D;                  // [kRB][kKT+1]
   uint32_t* masks = reinterpret_cast<uint32_t*>(ps + kRB * (kKT + 1));  // [128][4]
   __shared__ int tree_bad;
+  __shared__ int par_s[kMaxNodes];           // parent ids of the current tree
 
   __shared__ int cu_buf[512];
   Problem pr = a.pr;
@@ -72,9 +73,11 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
       __syncthreads();
       if (tid == 0) tree_bad = 0;
       __syncthreads();
+      for (int i = tid; i < s.m; i += kThreads) par_s[i] = __ldg(a.parent + s.n0 + i);  // one round of loads
+      __syncthreads();
       for (int i = tid; i < s.m; i += kThreads) {
         uint32_t bits[4];
-        if (!ancestor_bits(a.parent + s.n0, i, s.m, bits)) tree_bad = 1;
+        if (!ancestor_bits_shared(par_s, i, bits)) tree_bad = 1;
         masks[i * 4 + 0] = bits[0]; masks[i * 4 + 1] = bits[1];
         masks[i * 4 + 2] = bits[2]; masks[i * 4 + 3] = bits[3];
       }

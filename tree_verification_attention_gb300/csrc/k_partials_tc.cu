@@ -86,26 +86,6 @@ __device__ __forceinline__ bool next_segment(const Problem& pr, long long& t, lo
   return true;
 }
 
-// Ancestor-or-self bits of node i from the sequence's parent ids in shared memory.
-// False (only i's own bit set) when a parent met on the walk is outside [-1, node).
-__device__ __forceinline__ bool ancestor_bits_shared(const int* par, int i, uint32_t bits[4]) {
-  bits[0] = bits[1] = bits[2] = bits[3] = 0u;
-  bits[i >> 5] |= 1u << (i & 31);
-  int j = i;
-  for (int steps = 0; steps < kMaxNodes; ++steps) {
-    const int p = par[j];
-    if (p < -1 || p >= j) {
-      bits[0] = bits[1] = bits[2] = bits[3] = 0u;
-      bits[i >> 5] |= 1u << (i & 31);
-      return false;
-    }
-    if (p < 0) return true;
-    bits[p >> 5] |= 1u << (p & 31);
-    j = p;
-  }
-  return true;
-}
-
 // Q buffers: with one M-tile per row group (W = 1) the Q region holds two M-tiles, so
 // segments alternate between two buffers and the next segment's Q is loaded while the
 // current one is still in use; with W = 2 one buffer holds both M-tiles.

@@ -262,17 +262,17 @@ __device__ __forceinline__ GroupLoc locate_group(const Problem& pr, long long qg
   return R;
 }
 
-// Ancestor-or-self bit mask of tree node i (local id) over local ids 0..127:
-// mask bit c set iff node c is i or an ancestor of i.  Returns false if a parent id
-// met on the walk is outside [-1, node) (then only i's own bit is set).
-__device__ __forceinline__ bool ancestor_bits(const int32_t* parent_seq, int i, int m,
-                                              uint32_t bits[4]) {
+// Ancestor-or-self bit mask of tree node i (local id) over local ids 0..127, from the
+// sequence's parent ids staged in shared memory (`par`): bit c set iff node c is i or an
+// ancestor of i.  Returns false if a parent id met on the walk is outside [-1, node)
+// (then only i's own bit is set).
+__device__ __forceinline__ bool ancestor_bits_shared(const int* par, int i, uint32_t bits[4]) {
   bits[0] = bits[1] = bits[2] = bits[3] = 0u;
   bits[i >> 5] |= 1u << (i & 31);
   int j = i;
   for (int steps = 0; steps < kMaxNodes; ++steps) {
-    int p = __ldg(parent_seq + j);
-    if (p < -1 || p >= j || p >= m) {
+    const int p = par[j];
+    if (p < -1 || p >= j) {
       bits[0] = bits[1] = bits[2] = bits[3] = 0u;
       bits[i >> 5] |= 1u << (i & 31);
       return false;
