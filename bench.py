@@ -59,6 +59,15 @@ def algorithmic_flops(w):
     return f
 
 
+def l2_streams(mode, input_bytes, l2_bytes):
+    """Whether timed steps run without an L2 flush between them: forced by `mode`
+    ("stream" / "flush"), or ("auto") when a step's inputs exceed 1.5x the L2, so that
+    none of them can still be cached when the next step reads them."""
+    if mode in ("stream", "flush"):
+        return mode == "stream"
+    return input_bytes > 3 * l2_bytes // 2
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -290,7 +299,7 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
     input_bytes = algorithmic_bytes(w)[1]
-    stream_l2 = args.l2 == "stream" or (args.l2 == "auto" and input_bytes > 3 * l2_bytes // 2)
+    stream_l2 = l2_streams(args.l2, input_bytes, l2_bytes)
     dither = np.random.default_rng(12345)
 
     def between_steps(i):
