@@ -153,15 +153,20 @@ long long max_row_groups(const Problem& pr) {
   return (long long)pr.B * pr.Hkv * (((long long)pr.max_nodes * pr.G + pr.RG - 1) / pr.RG);
 }
 
-int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, v = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return 1;
-    n = v > 0 ? v : 1;
+constexpr int kMaxDevices = 64;
+
+// SMs of the current device (cached per device); 0 if it cannot be read.
+int sm_count(int* dev_out) {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  *dev_out = dev;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 0;
+    cache[dev] = v;
   }
-  return n;
+  return cache[dev];
 }
 
 // WPB warps per block: as many as keep the registers of two blocks per SM or more.  One
@@ -173,13 +178,15 @@ cudaError_t launch_typed(const CombineArgs& a, cudaStream_t s) {
   constexpr int WPB = CG == 1 ? 8 : 4;
   const int RGP = padded_group_rows(a.pr.RG, a.pr.G);
   const long long warps = max_row_groups(a.pr) * (RGP / 32) * (D / 4 / CG);
-  static int per_sm = 0;
-  if (per_sm == 0 &&
-      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<T, D, CG, NB, WPB>, 32 * WPB, 0) !=
-           cudaSuccess ||
-       per_sm < 1))
-    per_sm = 1;
-  const long long wave = (long long)sm_count() * per_sm;
+  static int per_sm[kMaxDevices] = {0};  // resident blocks per SM, per device
+  int dev = 0;
+  const int sms = sm_count(&dev);
+  if (sms > 0 && per_sm[dev] == 0) {
+    int v = 0;
+    per_sm[dev] = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, combine_kernel<T, D, CG, NB, WPB>, 32 * WPB, 0) ==
+                              cudaSuccess && v > 0 ? v : 1;
+  }
+  const long long wave = sms > 0 ? (long long)sms * per_sm[dev] : 0;
   long long blocks = (warps + WPB - 1) / WPB;
   if (blocks < wave) blocks = std::min<long long>(wave, warps);
   if (blocks <= 0) return cudaSuccess;
