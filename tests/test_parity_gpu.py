@@ -50,6 +50,10 @@ EDGE = [
     # GQA groups that do not divide 128: M-tiles of 126 / 125 rows, padded in the partials
     dict(batch=2, Hq=12, Hkv=4, d=128, prefix=(77, 200), m=50, tree="random", dtype="bf16", vocab=8),
     dict(batch=1, Hq=10, Hkv=2, d=64, prefix=300, m=30, tree="random", dtype="fp32", vocab=8),
+    # many short sequences: every worker crosses two or three row groups, so consecutive
+    # segments alternate between the two Q buffers of one-M-tile row groups
+    dict(batch=40, Hq=32, Hkv=8, d=128, prefix=(50, 300), m=8, tree="random", dtype="bf16", vocab=8),
+    dict(batch=24, Hq=16, Hkv=4, d=64, prefix=(0, 260), m=12, tree="random", dtype="fp16", vocab=8),
     # float16 (LongSpec's precision): d = 64 and 128, a ragged batch, a full 128-node tree
     dict(batch=3, Hq=8, Hkv=2, d=64, prefix=(0, 400), m=21, tree="random", dtype="fp16", vocab=8),
     dict(batch=1, Hq=32, Hkv=8, d=128, prefix=300, m=128, tree="random", dtype="fp16", vocab=8),
