@@ -26,6 +26,17 @@ template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v
   return __bfloat162float(v);
 }
 
+// Four consecutive elements of a row (16-byte aligned for float: rows are D floats and
+// the base pointers are 16-byte aligned).
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p) {
+  if constexpr (sizeof(T) == 4) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+  } else {
+    return make_float4(to_f(p[0]), to_f(p[1]), to_f(p[2]), to_f(p[3]));
+  }
+}
+
 template <int D>
 constexpr size_t simt_smem_bytes() {
   return sizeof(float) * (kRB * (D + 1) + kKT * (D + 1) + kKT * D + kRB * (kKT + 1)) +
@@ -33,7 +44,7 @@ constexpr size_t simt_smem_bytes() {
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) partials_simt_kernel(PartialArgs a) {
   extern __shared__ float smem[];
   float* qs = smem;                          // [kRB][D+1]
   float* ks = qs + kRB * (D + 1);            // [kKT][D+1]
@@ -90,15 +101,23 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
     const int row_end = min(rows_total, row_begin + pr.RG);
     for (int rb = row_begin; rb < row_end; rb += kRB) {
       __syncthreads();
-      for (int idx = tid; idx < kRB * D; idx += kThreads) {
-        const int r = idx / D, dd = idx % D;
-        const int row = rb + r;
-        float v = 0.f;
-        if (row < row_end) {
-          const int i = row / pr.G, j = row % pr.G;
-          v = to_f(q[((size_t)(s.n0 + i) * pr.Hq + L.g * pr.G + j) * D + dd]);
+      {
+        // all of the thread's loads first (one round of latency), then the stores
+        constexpr int kN = kRB * D / 4 / kThreads;
+        float4 qv[kN];
+#pragma unroll
+        for (int i = 0; i < kN; ++i) {
+          const int idx = (tid + i * kThreads) * 4, r = idx / D, dd = idx % D, row = rb + r;
+          qv[i] = row < row_end
+                      ? load4(q + ((size_t)(s.n0 + row / pr.G) * pr.Hq + L.g * pr.G + row % pr.G) * D + dd)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        qs[r * (D + 1) + dd] = v;
+#pragma unroll
+        for (int i = 0; i < kN; ++i) {
+          const int idx = (tid + i * kThreads) * 4, r = idx / D, dd = idx % D;
+          float* dst = qs + r * (D + 1) + dd;
+          dst[0] = qv[i].x; dst[1] = qv[i].y; dst[2] = qv[i].z; dst[3] = qv[i].w;
+        }
       }
       const int my_row = rb + r_loc;
       const bool row_ok = my_row < row_end;
@@ -116,14 +135,30 @@ __global__ void __launch_bounds__(kThreads) partials_simt_kernel(PartialArgs a) 
         const size_t first = is_tree ? (size_t)s.n0 : (size_t)s.p0 + (size_t)(tile - 1) * kKeyTile;
         kb += first * kv_stride + (size_t)L.g * D;
         vb += first * kv_stride + (size_t)L.g * D;
+        // The sub-tile's K / V are loaded into registers one sub-tile ahead: the loads
+        // of sub-tile k0 + kKT are in flight while sub-tile k0 is computed.
+        constexpr int kN = kKT * D / 4 / kThreads;
+        float4 kr[kN], vr[kN];
+        auto fetch = [&](int k0) {
+#pragma unroll
+          for (int i = 0; i < kN; ++i) {
+            const int idx = (tid + i * kThreads) * 4, key = idx / D, dd = idx % D;
+            const bool valid = k0 + key < nkeys;
+            kr[i] = valid ? load4(kb + (size_t)(k0 + key) * kv_stride + dd) : make_float4(0.f, 0.f, 0.f, 0.f);
+            vr[i] = valid ? load4(vb + (size_t)(k0 + key) * kv_stride + dd) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        };
+        fetch(0);
         for (int k0 = 0; k0 < nkeys; k0 += kKT) {
           __syncthreads();
-          for (int idx = tid; idx < kKT * D; idx += kThreads) {
-            const int key = idx / D, dd = idx % D;
-            const bool valid = k0 + key < nkeys;
-            ks[key * (D + 1) + dd] = valid ? to_f(kb[(size_t)(k0 + key) * kv_stride + dd]) : 0.f;
-            vs[key * D + dd] = valid ? to_f(vb[(size_t)(k0 + key) * kv_stride + dd]) : 0.f;
+#pragma unroll
+          for (int i = 0; i < kN; ++i) {
+            const int idx = (tid + i * kThreads) * 4, key = idx / D, dd = idx % D;
+            float* kd = ks + key * (D + 1) + dd;
+            kd[0] = kr[i].x; kd[1] = kr[i].y; kd[2] = kr[i].z; kd[3] = kr[i].w;
+            *reinterpret_cast<float4*>(vs + key * D + dd) = vr[i];
           }
+          if (k0 + kKT < nkeys) fetch(k0 + kKT);
           __syncthreads();
           float sc[4];
 #pragma unroll
