@@ -2,8 +2,10 @@
 //
 // One CTA per worker of the unit decomposition in tva_common.cuh.  For every segment
 // (a contiguous run of key tiles of one row group) the CTA walks the row group in
-// blocks of 32 rows; per block it streams the segment's keys in sub-tiles of 32 and
-// keeps a running maximum / sum per row (online softmax, base 2), so each segment
+// blocks of 32 rows; per block it streams the segment's keys in sub-tiles of 32 (each
+// thread's share fetched as 16-byte vectors one sub-tile ahead, so the loads of the
+// next sub-tile overlap the work on this one) and keeps a running maximum / sum per
+// row (online softmax, base 2), so each segment
 // yields the partial output O and log-sum-exp LSE of the LongSpec aggregation
 // ("Fast Tree Attention", Aggregation).  The tree tile is masked with the
 // ancestor-or-self bits of each row's node (LongSpec's tree mask; "Faster decoding",
