@@ -16,9 +16,13 @@
 // A sequence is served by a cluster of kCluster CTAs.  Every CTA repeats the cheap
 // acceptance tests (so all of them take the same decisions from the same inputs and
 // reach the cluster barriers together), then sums the quantised masses of its slice of
-// the vocabulary row with many loads in flight.  The slice sums are exchanged through
-// distributed shared memory; in the CTA whose slice holds the threshold an exclusive
-// scan of the per-thread chunk sums picks the chunk, and one thread walks it.
+// the vocabulary row with many loads in flight.  The slice is cut into one contiguous
+// chunk per warp, and a warp reads its chunk with coalesced 16-byte loads (lane l takes
+// every 32nd group of 4 entries), so each load instruction covers 512 contiguous bytes.
+// The slice sums are exchanged through distributed shared memory; in the CTA whose
+// slice holds the threshold the warp sums locate the warp chunk, whose lanes then take
+// contiguous pieces of it: a warp scan of their sums picks the piece, and one lane walks
+// it entry by entry.
 #include <cooperative_groups.h>
 
 #include "tc_ptx.cuh"
@@ -40,7 +44,6 @@ __device__ __forceinline__ unsigned long long quant(float w) {
   // w * 2^40 is exact (a power-of-two scale); truncation is the floor for w >= 0
   return __float2ull_rz(fmaxf(w, 0.f) * kQScale);
 }
-
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -56,21 +59,8 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
   return x;
 }
 
-// Block-wide sum of two u64 values per thread (result in every thread).
-__device__ __forceinline__ void block_sum2(unsigned long long& a, unsigned long long& b,
-                                           unsigned long long* s) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  a = warp_sum_u64(a);
-  b = warp_sum_u64(b);
-  if (lane == 0) { s[warp] = a; s[kWarps + warp] = b; }
-  __syncthreads();
-  a = 0; b = 0;
-  for (int w = 0; w < kWarps; ++w) { a += s[w]; b += s[kWarps + w]; }
-  __syncthreads();
-}
-
 struct __align__(16) ClusterShared {
-  unsigned long long red[2 * kWarps];
+  unsigned long long red[2 * kWarps];   // per-warp sums: residual masses, then p
   unsigned long long slice[2];   // this CTA's residual and p sums (read by the cluster)
   int first, tok;
 };
@@ -112,49 +102,79 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
   const float* prow = a.p + (size_t)(g0 + b + k) * a.V;
   const float* qrow = k < gamma ? a.q + (size_t)(g0 + k) * a.V : nullptr;
 
-  // ---- this CTA's slice, cut into contiguous per-thread chunks (multiples of 4 entries,
-  // read as 16-byte vectors when the rows are 16-byte aligned): chunk sums of the
-  // residual masses and of p
+  // ---- this CTA's slice, cut into one contiguous chunk per warp (a multiple of 128
+  // entries): per-warp sums of the residual masses and of p
   const int S = ((a.V + kCluster - 1) / kCluster + 3) & ~3;
   const int v0 = min(a.V, rank * S), v1 = min(a.V, v0 + S);
-  const int C = ((v1 - v0 + kThreads - 1) / kThreads + 3) & ~3;
-  const int c0 = min(v1, v0 + (int)threadIdx.x * C), c1 = min(v1, c0 + C);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int WC = ((v1 - v0 + kWarps - 1) / kWarps + 127) & ~127;
+  const int w0 = min(v1, v0 + warp * WC), w1 = min(v1, w0 + WC);
   // every row starts on a 16-byte boundary
   const bool vec = (a.V & 3) == 0 && ((reinterpret_cast<uintptr_t>(a.p) | reinterpret_cast<uintptr_t>(a.q)) & 15) == 0;
-  auto load4 = [&](const float* row, int v, float* out) {
-    if (vec && v + 3 < c1) {
+  auto load4 = [&](const float* row, int v, int end, float* out) {
+    if (vec && v + 3 < end) {
       const float4 t = __ldg(reinterpret_cast<const float4*>(row + v));
       out[0] = t.x; out[1] = t.y; out[2] = t.z; out[3] = t.w;
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) out[e] = v + e < c1 ? __ldg(row + v + e) : 0.f;
+      for (int e = 0; e < 4; ++e) out[e] = v + e < end ? __ldg(row + v + e) : 0.f;
     }
   };
-  unsigned long long cr = 0, cp = 0;   // this thread's chunk sums
-  for (int base = c0; base < c1; base += 4 * kUnroll) {
-    float pv[kUnroll][4], qv[kUnroll][4];
+  unsigned long long cr = 0, cp = 0;   // this lane's sums
+  auto accumulate = [&](const float (&pv)[4], const float (&qv)[4]) {
 #pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int v = base + 4 * j;
-      if (v < c1) {
-        load4(prow, v, pv[j]);
-        if (qrow != nullptr) load4(qrow, v, qv[j]);
-        else qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
-      } else {
-        pv[j][0] = pv[j][1] = pv[j][2] = pv[j][3] = 0.f;
-        qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
+    for (int e = 0; e < 4; ++e) {
+      cr += quant(fmaxf(0.f, __fsub_rn(pv[e], qv[e])));
+      cp += quant(pv[e]);
+    }
+  };
+  if (vec) {
+    // 16-byte rows with V a multiple of 4: every group of 4 starting below w1 is whole,
+    // so the loads are plain selects and all of them are issued before the first use
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = w0; base < w1; base += 128 * kUnroll) {
+      float4 p4[kUnroll], q4[kUnroll];
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int v = base + 128 * j + 4 * lane;
+        p4[j] = v < w1 ? __ldg(reinterpret_cast<const float4*>(prow + v)) : zero;
+        q4[j] = (v < w1 && qrow != nullptr) ? __ldg(reinterpret_cast<const float4*>(qrow + v)) : zero;
+      }
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const float pv[4] = {p4[j].x, p4[j].y, p4[j].z, p4[j].w};
+        const float qv[4] = {q4[j].x, q4[j].y, q4[j].z, q4[j].w};
+        accumulate(pv, qv);
       }
     }
+  } else {
+    for (int base = w0; base < w1; base += 128 * kUnroll) {
+      float pv[kUnroll][4], qv[kUnroll][4];
 #pragma unroll
-    for (int j = 0; j < kUnroll; ++j)
+      for (int j = 0; j < kUnroll; ++j) {
+        const int v = base + 128 * j + 4 * lane;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        cr += quant(fmaxf(0.f, __fsub_rn(pv[j][e], qv[j][e])));
-        cp += quant(pv[j][e]);
+        for (int e = 0; e < 4; ++e) {
+          pv[j][e] = v + e < w1 ? __ldg(prow + v + e) : 0.f;
+          qv[j][e] = (v + e < w1 && qrow != nullptr) ? __ldg(qrow + v + e) : 0.f;
+        }
       }
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) accumulate(pv[j], qv[j]);
+    }
   }
-  unsigned long long sr = cr, sp = cp;
-  block_sum2(sr, sp, sh.red);
+  cr = warp_sum_u64(cr);
+  cp = warp_sum_u64(cp);
+  if (lane == 0) {
+    sh.red[warp] = cr;
+    sh.red[kWarps + warp] = cp;
+  }
+  __syncthreads();
+  unsigned long long sr = 0, sp = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    sr += sh.red[w];
+    sp += sh.red[kWarps + w];
+  }
   if (threadIdx.x == 0) { sh.slice[0] = sr; sh.slice[1] = sp; }
   cluster.sync();   // every slice sum is visible to the cluster
 
@@ -183,43 +203,45 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
   const unsigned long long T = (__umul64hi(U, Z) << 40) | ((U * Z) >> 24);  // floor(U * Z / 2^24)
   if (!(before <= T && T < before + mine)) return;   // another CTA's slice holds the draw
 
-  // ---- the draw inside this slice: exclusive scan of the chunk sums, then the one
-  // chunk holding the threshold is read again and walked entry by entry
-  const unsigned long long cs = use_res ? cr : cp;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned long long incl = warp_incl_scan_u64(cs, lane);
-  if (lane == 31) sh.red[warp] = incl;
+  // ---- the draw inside this slice: the warp chunk holding the threshold (from the warp
+  // sums), then inside it the lanes take contiguous pieces; a warp scan of the pieces'
+  // sums picks the one holding the threshold, and its lane walks it entry by entry
   if (threadIdx.x == 0) sh.tok = -1;
   __syncthreads();
-  unsigned long long woff = 0;
-  for (int w = 0; w < warp; ++w) woff += sh.red[w];
-  const unsigned long long excl = before + woff + incl - cs;   // running sum before this chunk
-  if (excl <= T && T < excl + cs) {
-    unsigned long long run = excl;
-    int tok = -1;
-    for (int base = c0; base < c1 && tok < 0; base += 4 * kUnroll) {
-      float pv[kUnroll][4], qv[kUnroll][4];
+  const unsigned long long* wsum = use_res ? sh.red : sh.red + kWarps;
+  unsigned long long wexcl = before;
+  for (int w = 0; w < warp; ++w) wexcl += wsum[w];
+  if (wexcl <= T && T < wexcl + wsum[warp]) {   // uniform over the warp
+    const int LC = WC / 32;                      // entries per lane (a multiple of 4)
+    const int l0 = min(w1, w0 + lane * LC), l1 = min(w1, l0 + LC);
+    unsigned long long ls = 0;
+    for (int v = l0; v < l1; v += 4) {
+      float pv[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
+      load4(prow, v, l1, pv);
+      if (use_res) load4(qrow, v, l1, qv);
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
-        const int v = base + 4 * j;
-        if (v < c1) {
-          load4(prow, v, pv[j]);
-          if (use_res) load4(qrow, v, qv[j]);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
-        const int v = base + 4 * j;
+      for (int e = 0; e < 4; ++e)
+        ls += use_res ? quant(fmaxf(0.f, __fsub_rn(pv[e], qv[e]))) : quant(pv[e]);
+    }
+    const unsigned long long incl = warp_incl_scan_u64(ls, lane);
+    const unsigned long long lexcl = wexcl + incl - ls;   // running sum before this piece
+    if (lexcl <= T && T < lexcl + ls) {
+      unsigned long long run = lexcl;
+      int tok = -1;
+      for (int v = l0; v < l1 && tok < 0; v += 4) {
+        float pv[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
+        load4(prow, v, l1, pv);
+        if (use_res) load4(qrow, v, l1, qv);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          if (tok < 0 && v + e < c1) {
-            run += use_res ? quant(fmaxf(0.f, __fsub_rn(pv[j][e], qv[j][e]))) : quant(pv[j][e]);
+          if (tok < 0 && v + e < l1) {
+            run += use_res ? quant(fmaxf(0.f, __fsub_rn(pv[e], qv[e]))) : quant(pv[e]);
             if (run > T) tok = v + e;
           }
         }
       }
+      sh.tok = tok;
     }
-    sh.tok = tok;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
