@@ -44,6 +44,7 @@ __device__ __forceinline__ unsigned long long quant(float w) {
   // w * 2^40 is exact (a power-of-two scale); truncation is the floor for w >= 0
   return __float2ull_rz(fmaxf(w, 0.f) * kQScale);
 }
+
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
