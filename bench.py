@@ -160,6 +160,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over the ranks of the default process group (the
+    slowest rank sets each timing)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
 def dist_setup(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -379,9 +389,7 @@ def main():
     ms = float(np.mean(step_ms))
     k1 = float(np.mean(k1_ms))
     if world > 1:
-        t = torch.tensor([ms, k1], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, k1 = float(t[0]), float(t[1])
+        ms, k1 = max_over_ranks([ms, k1], dev)
 
     # ---- KV commit of the accepted path (a "next" row, measured on its own, outside the
     # step): the step's own acceptance result, appended to a reserved cache region.
@@ -495,9 +503,7 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
     if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+        (e2e_ms,) = max_over_ranks([e2e_ms], dev)
     if device_status() != 0:
         raise SystemExit(f"device status {device_status()}")
 
