@@ -8,12 +8,13 @@ prefix 65536, 64-node best-first tree (width 4, depth <= 8).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
 
 Prints one JSON line (rank 0).  `value` is tree nodes verified per second over all
-ranks (each rank runs its own copy of the workload: weak scaling).  Between timed
-steps either the L2 cache is flushed (256 MiB write, outside the timed interval) or,
-when the step's inputs are more than 1.5 times the L2 size, nothing is done: each step then
-streams inputs the L2 cannot hold (the previous step's leave it long before they are
-read again).  Each timed step starts after a GPU sleep of random length, so that the
-start falls at a random phase of the event timer's tick.
+ranks (each rank runs its own copy of the workload: weak scaling).  When a step's
+inputs are more than 1.5 times the L2 size, the K timed steps run back to back between
+one pair of CUDA events: each step streams inputs the L2 cannot hold (the previous
+step's leave it long before they are read again).  The same steps are also timed one
+at a time (each between its own events, after a GPU sleep of random length) and
+reported under "isolated".  Smaller workloads are timed one step at a time with the L2
+flushed (256 MiB write, outside the timed interval) before each.
 `--impl reference` times the CPU oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -205,6 +206,38 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), or the machine type when lscpu has none."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
+
+
+SINGLE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def single_thread_oracle(config):
+    """The oracle's nodes/s on the same bounded sample with its BLAS limited to one
+    thread (a child process, since BLAS reads the thread count when it loads)."""
+    env = dict(os.environ, **{k: "1" for k in SINGLE_THREAD_ENV})
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
+            "from tree_verification_attention_gb300 import workloads; "
+            "w = workloads.make_workload(%d); bench.cpu_oracle_sample(w, 1, 1); "
+            "dt, n = bench.cpu_oracle_sample(w, 1, 1); print(json.dumps([dt, n]))") % (ROOT, int(config))
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        dt, n = json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
+    return {"value": n / dt, "unit": "nodes/s", "cores": 1, "seconds_per_sample": dt}
+
+
 def run_reference(args, w, rank):
     if rank != 0:
         return
@@ -228,7 +261,7 @@ def run_reference(args, w, rank):
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                    "prefix_len": [int(x) for x in w.prefix_lens][:8], "tree_nodes": int(w.tree_sizes.max())},
         "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": sample},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -354,42 +387,58 @@ def main():
         raise SystemExit(f"device status {device_status()} during warm-up")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    evk = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid) if hasattr(
         torch.cuda.get_device_properties(dev), "uuid") else str(local)
     sampler = ClockSampler(gpu_id)
+
+    def timed(fn, offset):
+        """Mean milliseconds per call of `fn` over K calls.  When the inputs exceed 1.5x
+        the L2 the K calls run back to back between one pair of CUDA events (nothing of
+        one call's inputs is still cached when the next reads them); otherwise each
+        call has its own event pair, preceded by an untimed L2 flush.  Returns (mean ms,
+        per-call isolated ms or None)."""
+        torch.cuda._sleep(int(20e6))   # the host enqueues ahead of the GPU: no launch gaps
+        if stream_l2:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(K):
+                fn()
+            e1.record(stream)
+            # the same calls one at a time, each between its own events after a random
+            # GPU sleep (so each pays its own launch latency): reported beside the mean
+            evi = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+            for i in range(K):
+                between_steps(i + offset)
+                evi[i][0].record(stream)
+                fn()
+                evi[i][1].record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / K, float(np.mean([a.elapsed_time(b) for a, b in evi]))
+        evi = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            between_steps(i + offset)
+            evi[i][0].record(stream)
+            fn()
+            evi[i][1].record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in evi])), None
+
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.3)
-    # Whole steps.  The host enqueues ahead of the GPU (a GPU sleep first), so the
-    # timings hold no launch gaps; nothing separates the three kernels of a step.
-    torch.cuda._sleep(int(20e6))
-    for i in range(K):
-        between_steps(i)
-        ev[i][0].record(stream)
-        attn(d)
-        accept(d)
-        ev[i][1].record(stream)
-    # The dominant kernel alone (partials), same L2 handling, for the roofline figure.
-    torch.cuda._sleep(int(20e6))
-    for i in range(K):
-        between_steps(i + 7)
-        evk[i][0].record(stream)
-        step(d)
-        evk[i][1].record(stream)
+    # Whole steps (partials, combine, acceptance); nothing separates the kernels of a step.
+    ms, ms_iso = timed(lambda: (attn(d), accept(d)), 0)
+    # The attention alone (partials + combine), and the dominant kernel alone (partials).
+    att_ms, att_iso = timed(lambda: attn(d), 3)
+    k1, k1_iso = timed(lambda: step(d), 7)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    k1_ms = [evk[i][0].elapsed_time(evk[i][1]) for i in range(K)]
-    ms = float(np.mean(step_ms))
-    k1 = float(np.mean(k1_ms))
     if world > 1:
-        ms, k1 = max_over_ranks([ms, k1], dev)
+        ms, att_ms, k1 = max_over_ranks([ms, att_ms, k1], dev)
 
     # ---- KV commit of the accepted path (a "next" row, measured on its own, outside the
     # step): the step's own acceptance result, appended to a reserved cache region.
@@ -502,6 +551,19 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
+    # What the host link itself gives: the step's two large inputs copied from pinned
+    # memory in one transfer of the same total size, on the same stream.
+    big = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    big_d = torch.empty(h2d, dtype=torch.uint8, device=dev)
+    big_d.copy_(big, non_blocking=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(Ke):
+        big_d.copy_(big, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d_one_copy_gbs = h2d / (e0.elapsed_time(e1) / Ke * 1e-3) / 1e9
+    del big, big_d
     if world > 1:
         (e2e_ms,) = max_over_ranks([e2e_ms], dev)
     if device_status() != 0:
@@ -514,9 +576,12 @@ def main():
         reps = max(1, min(20, int(args.cpu_seconds / max(dt1, 1e-3))))
         dt, nodes = cpu_oracle_sample(w, 1, reps)
         cpu = {"value": nodes / dt, "unit": "nodes/s", "cores": cpu_cores(), "kind": "oracle",
+               "cpu_model": cpu_model(),
                "sample": f"{reps}x: all {w.num_nodes} nodes x the {w.num_q_heads // w.num_kv_heads} query heads "
                          f"of 1 of {w.num_kv_heads} KV heads (node count scaled by 1/{w.num_kv_heads}), "
                          f"float64 numpy, + acceptance walk"}
+        if args.cpu_seconds > 0.5:
+            cpu["single_thread"] = single_thread_oracle(args.config)
 
     if world > 1:
         dist.barrier()
@@ -530,8 +595,8 @@ def main():
     k1_gbs = k1_bytes / (k1 * 1e-3) / 1e9
     roof_s = max(total_bytes / (hbm_peak * 1e9), flops / (tc_peak * 1e12))
     l2_note = (f"not flushed: the {input_bytes / 1e6:.0f} MB of inputs each step streams exceed 1.5x the "
-               f"{l2_bytes / 1e6:.0f} MB L2" if stream_l2 else
-               "flushed before every timed step (256 MiB write, untimed)")
+               f"{l2_bytes / 1e6:.0f} MB L2, so the K steps run back to back between one event pair" if stream_l2 else
+               "flushed before every timed step (256 MiB write, untimed); one event pair per step")
     traffic = recorded_traffic(w.name)
     # The partials kernel's own bound: the slower of its bytes at the HBM peak and its
     # FLOPs at the bf16 tensor peak (the burst figure: the kernel is timed alone).
@@ -540,6 +605,7 @@ def main():
                     "kernel": "partials (prefix split-KV + tree tile)",
                     "traffic": traffic, "algorithmic_bytes": k1_bytes, "algorithmic_flops": flops,
                     "us_per_launch": k1 * 1e3,
+                    "us_per_launch_isolated": None if k1_iso is None else k1_iso * 1e3,
                     "timed": f"{K} launches of the partials kernel alone, " + l2_note}
     if tensor_bound:
         k1_tf = flops / (k1 * 1e-3) / 1e12
@@ -570,10 +636,18 @@ def main():
                    "l2": l2_note},
         "prefix_kv_gbs": prefix_kv / (ms * 1e-3) / 1e9,
         "step_roofline_frac": roof_s / (ms * 1e-3),
+        "attention_us": att_ms * 1e3,
+        "attention_roofline_frac": roof_s / (att_ms * 1e-3),
+        "isolated": None if ms_iso is None else {
+            "step_us": ms_iso * 1e3, "attention_us": att_iso * 1e3, "partials_us": k1_iso * 1e3,
+            "step_roofline_frac": roof_s / (ms_iso * 1e-3), "attention_roofline_frac": roof_s / (att_iso * 1e-3),
+            "timed": f"{K} calls one at a time, each between its own events after a random GPU sleep"},
         "roofline": roofline_obj,
         "cpu_baseline": cpu,
         "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "h2d_gbs_in_step": h2d / (e2e_ms * 1e-3) / 1e9,
+                "h2d_gbs_one_pinned_copy": h2d_one_copy_gbs},
         "kv_commit": {"us_per_launch": commit_ms * 1e3, "rows": committed_rows, "bytes": commit_bytes,
                       "gbs": commit_bytes / (commit_ms * 1e-3) / 1e9,
                       "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
@@ -583,7 +657,9 @@ def main():
         "gdn_tree": {"workload": "B=1, H=32, d=128, 64-node best-first tree, fp32", "us_per_launch": gdn_ms * 1e3,
                      "bytes": gdn_bytes, "gbs": gdn_bytes / (gdn_ms * 1e-3) / 1e9,
                      "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
-        "gpu_launches": 3 * K,
+        # this library's kernels in the timed region: steps (3 each), attention (2), partials (1);
+        # with streamed inputs each is timed back to back and once more one call at a time
+        "gpu_launches": (12 if stream_l2 else 6) * K,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -128,12 +128,16 @@ tva_status tree_verify_attn_combine(const tva_params* p, const void* workspace,
  * device memory (an engine that owns every allocation and forbids cudaMalloc on its
  * execution path, or a plugin interface with no workspace argument).  The paper has no
  * counterpart: this is a packaging of the same path.
- * Scratch: a fixed 32 MiB array compiled into the library, reserved on every GPU that
- * loads the library's device code and held until the process exits.  Problems whose
- * tva_workspace_size() exceeds 32 MiB are rejected with TVA_ERR_WORKSPACE (see
- * tva_last_error()) before anything is enqueued.  The first call on each device looks
- * the array's device address up (cudaGetSymbolAddress), so make that first call
- * before any stream capture.  Nothing here allocates.  All calls share the one array
+ * Scratch: a fixed 32 MiB array compiled into the library and held on each GPU until
+ * the process exits.  It is reserved when the module holding it is loaded on a device:
+ * with CUDA's default lazy module loading that happens at this entry point's first
+ * call on the device (with CUDA_MODULE_LOADING=EAGER, when the library's device code
+ * is loaded), and that first call fails with TVA_ERR_CUDA (see tva_last_error()) if
+ * the device has no 32 MiB left.  Problems whose tva_workspace_size() exceeds 32 MiB
+ * are rejected with TVA_ERR_WORKSPACE (see tva_last_error()) before anything is
+ * enqueued.  The first call on each device also looks the array's device address up
+ * (cudaGetSymbolAddress), so make that first call before any stream capture.  Nothing
+ * here calls an allocator.  All calls share the one array
  * and its contents carry over between calls (no step needs it zeroed); calls whose
  * work overlaps on the GPU (other streams, other host threads) race on it, so
  * serialise them.  Arguments otherwise as for tree_verify_attn_varlen. */
@@ -149,7 +153,10 @@ tva_status tree_verify_attn_varlen_noalloc(const tva_params* p, const void* q,
  * device (and grown when a larger problem arrives), released by tva_release().
  * Because it may allocate, do not call it for the first time inside stream capture.
  * Device-side errors go to a library-owned status word read by
- * tva_read_device_status(). */
+ * tva_read_device_status().  Every call on a device shares that device's one
+ * workspace: calls whose work overlaps on the GPU (several streams, several host
+ * threads) race on it, so serialise them (the varlen forms take a caller-owned
+ * workspace per call instead). */
 tva_status tree_verify_attn(const void* q, const void* k_cache, const void* v_cache,
                             int prefix_len, const void* tree_k, const void* tree_v,
                             const int32_t* parent, int num_nodes, int num_q_heads,
@@ -162,6 +169,17 @@ tva_status tva_read_device_status(int32_t* host_status, void* stream);
 
 /* Frees the convenience form's library-owned buffers on every device. */
 void tva_release(void);
+
+/* Diagnostics, for testing the device-side timeout path; not for production use.
+ * Sets, for this process and for launches made after the call, the limit of the
+ * main-loop waits inside the tensor-core attention partials kernel (bf16 / fp16) in
+ * nanoseconds (0 restores the default of 2 s).  With force_stall non-zero, that
+ * kernel's MMA-issuing thread first waits on a barrier that nothing completes, so the
+ * wait runs out: the kernel then raises its abort flag, lets every copy and MMA it
+ * started finish (those drain waits always keep the 2 s limit), frees its tensor
+ * memory, returns, and TVA_ERR_TIMEOUT is written to *dev_status.  Outputs of such a
+ * launch are unspecified.  Call tva_diag_set_wait_limit(0, 0) to return to normal. */
+void tva_diag_set_wait_limit(unsigned long long wait_limit_ns, int force_stall);
 
 /* Greedy longest accepted path per sequence ("Faster decoding", greedy contract).
  *   cu_nodes      [B+1] device, as in tva_params

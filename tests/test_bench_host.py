@@ -88,3 +88,9 @@ def test_reference_arm_prints_the_contract_line():
     assert line["cpu_baseline"]["value"] == line["value"] and line["cpu_baseline"]["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": "nodes/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_cpu_baseline_records_the_host_model_and_a_single_thread_figure():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+    one = bench.single_thread_oracle(2)
+    assert one is not None and one["cores"] == 1 and one["value"] > 0 and one["unit"] == "nodes/s"

@@ -5,12 +5,13 @@ and forbids cudaMalloc on its execution path, or a plugin interface with no work
 argument - call this form; its scratch is a fixed 32 MiB array inside the library.
 This file is collected last on purpose.  It checks, through the C ABI, that two calls
 in a row (on different problems, so the second one starts from the first one's
-leftover scratch) match the workspace form within the parity tolerances, and that a
-problem too large for the fixed scratch is refused before anything runs.
+leftover scratch) match the float64 oracle within the parity tolerances and are bit
+for bit the workspace form's results (the same kernels, layout and reduction order run
+on both, so any difference would be stale scratch leaking in), and that a problem too
+large for the fixed scratch is refused before anything runs.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -32,17 +33,19 @@ def _both(w):
             t["cu_nodes"], max(1, int(w.prefix_lens.max())), int(w.tree_sizes.max()))
     st_ref = torch.zeros(1, dtype=torch.int32, device="cuda:0")
     st_new = torch.zeros(1, dtype=torch.int32, device="cuda:0")
-    o_ref, l_ref = api.tree_verify_attn_varlen(*args, dev_status=st_ref)
     o_new, l_new = api.tree_verify_attn_varlen_noalloc(*args, dev_status=st_new)
+    o_ws, l_ws = api.tree_verify_attn_varlen(*args, dev_status=st_ref)
     torch.cuda.synchronize()
     assert int(st_ref.item()) == 0 and int(st_new.item()) == 0
-    return [x.double().cpu().numpy() for x in (o_new, l_new, o_ref, l_ref)]
+    return o_new, l_new, o_ws, l_ws
 
 
-def test_two_calls_in_a_row_match_the_workspace_form():
+def test_two_calls_in_a_row_match_the_oracle_and_the_workspace_form():
     for w in (workloads.make_workload(3, prefix=1500), workloads.make_workload(4, prefix=(200, 1300))):
-        o_new, l_new, o_ref, l_ref = _both(w)
-        _gpu.assert_close(w, o_new, l_new, o_ref, l_ref, w.name)
+        o_new, l_new, o_ws, l_ws = _both(w)
+        o_ref, l_ref = _gpu.oracle_attention(w)
+        _gpu.assert_close(w, o_new.double().cpu().numpy(), l_new.double().cpu().numpy(), o_ref, l_ref, w.name)
+        assert torch.equal(o_new, o_ws) and torch.equal(l_new, l_ws), w.name
 
 
 def test_too_large_for_the_static_scratch_is_refused():

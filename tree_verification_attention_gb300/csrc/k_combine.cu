@@ -22,6 +22,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "tc_ptx.cuh"
@@ -157,16 +158,17 @@ constexpr int kMaxDevices = 64;
 
 // SMs of the current device (cached per device); 0 if it cannot be read.
 int sm_count(int* dev_out) {
-  static int cache[kMaxDevices] = {0};
+  // Filled on first use per device; concurrent first calls store the same value.
+  static std::atomic<int> cache[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   *dev_out = dev;
-  if (cache[dev] == 0) {
-    int v = 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return 0;
-    cache[dev] = v;
+    cache[dev].store(v, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return v;
 }
 
 // WPB warps per block: as many as keep the registers of two blocks per SM or more.  One
@@ -178,15 +180,17 @@ cudaError_t launch_typed(const CombineArgs& a, cudaStream_t s) {
   constexpr int WPB = CG == 1 ? 8 : 4;
   const int RGP = padded_group_rows(a.pr.RG, a.pr.G);
   const long long warps = max_row_groups(a.pr) * (RGP / 32) * (D / 4 / CG);
-  static int per_sm[kMaxDevices] = {0};  // resident blocks per SM, per device
+  static std::atomic<int> per_sm[kMaxDevices];  // resident blocks per SM, per device (0: not yet known)
   int dev = 0;
   const int sms = sm_count(&dev);
-  if (sms > 0 && per_sm[dev] == 0) {
+  int resident = sms > 0 ? per_sm[dev].load(std::memory_order_relaxed) : 0;
+  if (sms > 0 && resident == 0) {
     int v = 0;
-    per_sm[dev] = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, combine_kernel<T, D, CG, NB, WPB>, 32 * WPB, 0) ==
-                              cudaSuccess && v > 0 ? v : 1;
+    resident = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, combine_kernel<T, D, CG, NB, WPB>, 32 * WPB, 0) ==
+                           cudaSuccess && v > 0 ? v : 1;
+    per_sm[dev].store(resident, std::memory_order_relaxed);
   }
-  const long long wave = sms > 0 ? (long long)sms * per_sm[dev] : 0;
+  const long long wave = sms > 0 ? (long long)sms * resident : 0;
   long long blocks = (warps + WPB - 1) / WPB;
   if (blocks < wave) blocks = std::min<long long>(wave, warps);
   if (blocks <= 0) return cudaSuccess;

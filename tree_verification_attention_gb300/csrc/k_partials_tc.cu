@@ -8,13 +8,16 @@
 // one more 128-key tile whose logits are masked with the row's ancestor bits.
 //
 // How (one CTA per SM, 320 threads):
-//   warp 8  (producer): TMA loads of Q (once per segment; with one M-tile per row group
+//   warp 8  (producer): TMA loads, issued like the MMAs (below) by one elected lane of
+//           the converged warp, of Q (once per segment; with one M-tile per row group
 //           into two alternating buffers, so a worker's next segment does not wait for
 //           the current one's Q to be released) and of the K / V tiles into a ring of
 //           shared-memory stages, 128-byte swizzled.
-//   warp 9  (MMA):      single-thread tcgen05.mma issue.  S = Q K^T (both operands in
-//           shared memory) into TMEM; O += P V with P read from TMEM (P overwrites
-//           the first half of its S buffer as packed bf16) and V from shared memory.
+//   warp 9  (MMA):      tcgen05.mma issue.  The warp runs this role converged and one
+//           elected lane issues each MMA and commit (single-lane issue from a divergent
+//           branch was the kernel's bottleneck).  S = Q K^T (both operands in shared
+//           memory) into TMEM; O += P V with P read from TMEM (P overwrites the first
+//           half of its S buffer as packed bf16) and V from shared memory.
 //   warps 0-7 (softmax): two streams of 4 warps; thread r of a stream owns TMEM lane
 //           (= query row) r, so row max / sum need no shuffles.  A stream's running
 //           max is only moved when it grows by more than 2^8 (stale maxima cancel in
@@ -28,12 +31,13 @@
 // S is ready.
 // TMEM columns: S/P buffers at 0 and 128, O accumulators at 256 and 384 (512 total).
 //
-// Every wait is bounded (2 s): on expiry the CTA raises an abort flag, records
-// TVA_ERR_TIMEOUT, drains its in-flight copies and MMAs (bounded again), frees TMEM
-// and returns.
+// Every wait is bounded (2 s by default; the main-loop limit is a launch argument): on
+// expiry the CTA raises an abort flag, records TVA_ERR_TIMEOUT, drains its in-flight
+// copies and MMAs (bounded again, always with the full 2 s), frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdio>
 
 #include "tc_ptx.cuh"
@@ -47,7 +51,7 @@ using namespace ptx;
 constexpr int kThreadsTc = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kDrainNs = 2000000000ull;  // drain waits, and the default main-loop limit
 constexpr int kHalfBytes = 128 * 128;  // 128 rows of 64 bf16 (one 128-byte swizzle span)
 constexpr uint32_t kNegInfBits = 0xff800000u;
 
@@ -68,7 +72,13 @@ struct TcArgs {
   PartialArgs a;
   int W;    // M-tiles per row group (1 or 2)
   int npt;  // nodes per M-tile: floor(128 / G)
+  uint64_t wait_ns;  // limit of every main-loop wait
+  int stall;         // test hook: the MMA thread first waits on a barrier nothing completes
 };
+
+// Process-wide diagnostic settings (tva_diag_set_wait_limit): 0 = the default limit.
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+std::atomic<int> g_force_stall{0};
 
 struct Segment {
   Loc L;
@@ -93,10 +103,16 @@ __device__ __forceinline__ int q_buffer(int W, int sg) { return W == 1 ? (sg & 1
 // Earlier segments that used the same buffer.
 __device__ __forceinline__ int q_use(int W, int sg) { return W == 1 ? (sg >> 1) : sg; }
 
+// A bounded wait taken by a whole converged warp; the result is the same in every lane.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit_ns));
+}
+
 // Waits that ignore the abort flag (used only while draining).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   volatile int never = 0;
-  mbar_wait(bar, parity, &never, kWaitNs);
+  mbar_wait(bar, parity, &never, kDrainNs);
 }
 
 template <int D, bool kBF16>
@@ -114,6 +130,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   Problem* pr_s = reinterpret_cast<Problem*>(smem + C::kBarOff + C::kCuOff - 128);
   const Problem& pr = *pr_s;
   const int W = args.W, npt = args.npt, G = a.pr.G;  // kernel parameters: readable before staging
+  const uint64_t wait_ns = args.wait_ns;  // main-loop waits; drains use kDrainNs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u = blockIdx.x;
 
@@ -199,7 +216,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------------ producer
-    if (lane == 0) {
+    // All 32 lanes run this role; one elected lane issues each copy and expect-tx.
+    {
       int ring = 0, sg = 0;
       bool ok = true;
       long long t = t_begin;
@@ -209,24 +227,24 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       while (ok && next_segment(pr, t, t_end, S)) {
         const Loc& L = S.L;
         const int qb = q_buffer(W, sg), quse = q_use(W, sg);
-        if (quse > 0 && !mbar_wait(Q_EMPTY + 8 * qb, (quse - 1) & 1, abort_flag, kWaitNs)) { ok = false; break; }
-        mbar_expect_tx(Q_FULL + 8 * qb, (uint32_t)W * C::kHalves * q_box_bytes);
+        if (quse > 0 && !warp_wait(Q_EMPTY + 8 * qb, (quse - 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
+        mbar_expect_tx_elect(Q_FULL + 8 * qb, (uint32_t)W * C::kHalves * q_box_bytes);
         for (int mt = 0; mt < W; ++mt)
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(q_s + ((qb + mt) * C::kHalves + h) * kHalfBytes, &tm_q, 64 * h, L.g * G,
+            tma_load_3d_elect(q_s + ((qb + mt) * C::kHalves + h) * kHalfBytes, &tm_q, 64 * h, L.g * G,
                         L.s.n0 + (L.mp * W + mt) * npt, Q_FULL + 8 * qb);
         const int n = S.n;
         auto load = [&](int k, bool is_v) -> bool {
           const int stage = ring % C::kStages, use = ring / C::kStages;
-          if (use > 0 && !mbar_wait(KV_EMPTY + 8 * stage, (use - 1) & 1, abort_flag, kWaitNs))
+          if (use > 0 && !warp_wait(KV_EMPTY + 8 * stage, (use - 1) & 1, abort_flag, wait_ns))
             return false;
           const int tile = S.tile0 + k;
           const bool tree = tile == 0;
           const CUtensorMap* m = tree ? (is_v ? &tm_tv : &tm_tk) : (is_v ? &tm_v : &tm_k);
           const int z = tree ? L.s.n0 : L.s.p0 + (tile - 1) * kKeyTile;
-          mbar_expect_tx(KV_FULL + 8 * stage, C::kTileBytes);
+          mbar_expect_tx_elect(KV_FULL + 8 * stage, C::kTileBytes);
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d_hint(kv_s + stage * C::kTileBytes + h * kHalfBytes, m, 64 * h, L.g, z,
+            tma_load_3d_hint_elect(kv_s + stage * C::kTileBytes + h * kHalfBytes, m, 64 * h, L.g, z,
                              KV_FULL + 8 * stage, evict_first);
           ++ring;
           return true;
@@ -253,7 +271,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // All 32 lanes run this role (waits and descriptor arithmetic are warp-uniform);
+    // the *_elect forms issue each MMA / commit from one lane.
+    {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, kBF16);
       constexpr uint32_t idesc_o = idesc_bf16(128, D, true, kBF16);
       int ring = 0, sg = 0;
@@ -262,7 +282,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       long long t = t_begin;
       Segment S;
       auto wait_kv = [&](int idx) -> bool {
-        if (!mbar_wait(KV_FULL + 8 * (idx % C::kStages), (idx / C::kStages) & 1, abort_flag, kWaitNs))
+        if (!warp_wait(KV_FULL + 8 * (idx % C::kStages), (idx / C::kStages) & 1, abort_flag, wait_ns))
           return false;
         tc_fence_after();
         return true;
@@ -283,41 +303,44 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t o = (uint32_t)((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
-          mma_ss(dt, desc_join(ql + o, k_hi), desc_join(kl + o, k_hi), idesc_s, ks > 0);
+          mma_ss_elect(dt, desc_join(ql + o, k_hi), desc_join(kl + o, k_hi), idesc_s, ks > 0);
         }
-        tc_commit(S_FULL + 8 * w);
+        tc_commit_elect(S_FULL + 8 * w);
       };
       auto issue_pv = [&](int w, int idx, bool acc) {
         const uint32_t vl = v_lo + (uint32_t)((idx % C::kStages) * C::kTileBytes >> 4);
         const uint32_t dt = tmem + 256 + w * 128, at = tmem + w * 128;
 #pragma unroll
         for (int ks = 0; ks < kKeyTile / 16; ++ks)
-          mma_ts(dt, at + ks * 8, desc_join(vl + (uint32_t)(ks * 2048 >> 4), v_hi), idesc_o,
+          mma_ts_elect(dt, at + ks * 8, desc_join(vl + (uint32_t)(ks * 2048 >> 4), v_hi), idesc_o,
                  (acc || ks > 0) ? 1u : 0u);
       };
       auto wait_p = [&](int w) -> bool {
-        if (!mbar_wait(P_FULL + 8 * w, (pbits >> w) & 1u, abort_flag, kWaitNs)) return false;
+        if (!warp_wait(P_FULL + 8 * w, (pbits >> w) & 1u, abort_flag, wait_ns)) return false;
         tc_fence_after();
         return true;
       };
       auto wait_ofree = [&]() -> bool {
         if (sg == 0) return true;
-        if (!mbar_wait(O_FREE, (sg - 1) & 1, abort_flag, kWaitNs)) return false;
+        if (!warp_wait(O_FREE, (sg - 1) & 1, abort_flag, wait_ns)) return false;
         tc_fence_after();
         return true;
       };
+      // Test hook: DRAIN's first phase completes only through this thread's own commit
+      // below, so this wait runs out, exercising the timeout path (abort, drain, free).
+      if (args.stall && !warp_wait(DRAIN, 0, abort_flag, wait_ns)) ok = false;
       while (ok && next_segment(pr, t, t_end, S)) {
         const int n = S.n;
         qb = q_buffer(W, sg);
-        if (!mbar_wait(Q_FULL + 8 * qb, q_use(W, sg) & 1, abort_flag, kWaitNs)) { ok = false; break; }
+        if (!warp_wait(Q_FULL + 8 * qb, q_use(W, sg) & 1, abort_flag, wait_ns)) { ok = false; break; }
         tc_fence_after();
         if (W == 2) {
           // ring: K_k at ring + 2k, V_k at ring + 2k + 1
           if (!(ok = wait_kv(ring))) break;
           issue_s(0, 0, ring);
           issue_s(1, 1, ring);
-          tc_commit(KV_EMPTY + 8 * (ring % C::kStages));
-          if (n == 1) tc_commit(Q_EMPTY + 8 * qb);
+          tc_commit_elect(KV_EMPTY + 8 * (ring % C::kStages));
+          if (n == 1) tc_commit_elect(Q_EMPTY + 8 * qb);
           for (int k = 0; k < n && ok; ++k) {
             const int vi = ring + 2 * k + 1, ki = ring + 2 * k + 2;
             if (!(ok = wait_kv(vi))) break;
@@ -326,14 +349,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
               if (k == 0 && w == 0 && !(ok = wait_ofree())) break;
               issue_pv(w, vi, k > 0);
               pbits ^= 1u << w;
-              if (k == n - 1) tc_commit(O_FULL + 8 * w);
-              if (w == 1) tc_commit(KV_EMPTY + 8 * (vi % C::kStages));
+              if (k == n - 1) tc_commit_elect(O_FULL + 8 * w);
+              if (w == 1) tc_commit_elect(KV_EMPTY + 8 * (vi % C::kStages));
               if (k + 1 < n) {
                 if (w == 0 && !(ok = wait_kv(ki))) break;
                 issue_s(w, w, ki);
                 if (w == 1) {
-                  tc_commit(KV_EMPTY + 8 * (ki % C::kStages));
-                  if (k + 1 == n - 1) tc_commit(Q_EMPTY + 8 * qb);
+                  tc_commit_elect(KV_EMPTY + 8 * (ki % C::kStages));
+                  if (k + 1 == n - 1) tc_commit_elect(Q_EMPTY + 8 * qb);
                 }
               }
             }
@@ -344,13 +367,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           auto rV = [&](int j) { return ring + (j <= n - 2 ? 2 + 2 * j : 2 * n - 1); };
           if (!(ok = wait_kv(rK(0)))) break;
           issue_s(0, 0, rK(0));
-          tc_commit(KV_EMPTY + 8 * (rK(0) % C::kStages));
+          tc_commit_elect(KV_EMPTY + 8 * (rK(0) % C::kStages));
           if (n > 1) {
             if (!(ok = wait_kv(rK(1)))) break;
             issue_s(1, 0, rK(1));
-            tc_commit(KV_EMPTY + 8 * (rK(1) % C::kStages));
+            tc_commit_elect(KV_EMPTY + 8 * (rK(1) % C::kStages));
           }
-          if (n <= 2) tc_commit(Q_EMPTY + 8 * qb);
+          if (n <= 2) tc_commit_elect(Q_EMPTY + 8 * qb);
           for (int j = 0; j < n && ok; ++j) {
             const int w = j & 1;
             if (!(ok = wait_kv(rV(j)))) break;
@@ -358,13 +381,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             if (j == 0 && !(ok = wait_ofree())) break;
             issue_pv(w, rV(j), j >= 2);
             pbits ^= 1u << w;
-            tc_commit(KV_EMPTY + 8 * (rV(j) % C::kStages));
-            if (j + 2 >= n) tc_commit(O_FULL + 8 * w);
+            tc_commit_elect(KV_EMPTY + 8 * (rV(j) % C::kStages));
+            if (j + 2 >= n) tc_commit_elect(O_FULL + 8 * w);
             if (j + 2 < n) {
               if (!(ok = wait_kv(rK(j + 2)))) break;
               issue_s(w, 0, rK(j + 2));
-              tc_commit(KV_EMPTY + 8 * (rK(j + 2) % C::kStages));
-              if (j + 2 == n - 1) tc_commit(Q_EMPTY + 8 * qb);
+              tc_commit_elect(KV_EMPTY + 8 * (rK(j + 2) % C::kStages));
+              if (j + 2 == n - 1) tc_commit_elect(Q_EMPTY + 8 * qb);
             }
           }
         }
@@ -372,7 +395,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         ++sg;
       }
       // drain: every MMA issued by this thread has completed before TMEM is freed
-      tc_commit(DRAIN);
+      tc_commit_elect(DRAIN);
       drain_wait(DRAIN, 0);
     }
   } else {
@@ -402,7 +425,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         int* ps = par_s + w * 128;
         if (r < L.s.m) ps[r] = __ldg(a.parent + L.s.n0 + r);
         mbar_arrive(PAR_READY + 8 * w);
-        ok = __all_sync(0xffffffffu, mbar_wait(PAR_READY + 8 * w, trees & 1, abort_flag, kWaitNs));
+        ok = __all_sync(0xffffffffu, mbar_wait(PAR_READY + 8 * w, trees & 1, abort_flag, wait_ns));
         ++trees;
         if (!ok) break;
         if (row_ok && !ancestor_bits_shared(ps, node, anc)) set_status(a.status, kStatusBadTree);
@@ -413,7 +436,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int k = (W == 2) ? i : 2 * i + w;
         const int tile = S.tile0 + k;
         const bool is_tree = tile == 0;
-        ok = __all_sync(0xffffffffu, mbar_wait(S_FULL + 8 * w, cnt & 1, abort_flag, kWaitNs));
+        ok = __all_sync(0xffffffffu, mbar_wait(S_FULL + 8 * w, cnt & 1, abort_flag, wait_ns));
         if (!ok) break;
         tc_fence_after();
         // keys of this tile: [0, lim) exist; the tree tile also needs the ancestor bit
@@ -521,7 +544,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       const int pp = mt * 128 + r;  // padded row: lane = row within a 32-row block
       float* oblk = a.o_part + o_part_offset(slot, pp, 0, W * 128, D);
       if (W == 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8 * w, (w == 0 ? of0 : of1) & 1, abort_flag, kWaitNs));
+        ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8 * w, (w == 0 ? of0 : of1) & 1, abort_flag, wait_ns));
         if (!ok) break;
         (w == 0 ? of0 : of1)++;
         tc_fence_after();
@@ -547,7 +570,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         // before the O_FREE wait), so nothing else keeps it from arriving for
         // segment sg before segment sg-1's release completed: wait for that first.
         if (sg > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(O_FREE, (sg - 1) & 1, abort_flag, kWaitNs));
+          ok = __all_sync(0xffffffffu, mbar_wait(O_FREE, (sg - 1) & 1, abort_flag, wait_ns));
           if (!ok) break;
         }
         m1_s[(sg & 1) * 128 + r] = m_run;
@@ -555,16 +578,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         mbar_arrive(M1_READY);
         mbar_arrive(O_FREE);
       } else {
-        ok = __all_sync(0xffffffffu, mbar_wait(M1_READY, sg & 1, abort_flag, kWaitNs));
+        ok = __all_sync(0xffffffffu, mbar_wait(M1_READY, sg & 1, abort_flag, wait_ns));
         if (!ok) break;
         const float m1 = m1_s[(sg & 1) * 128 + r];
         const float l1 = l1_s[(sg & 1) * 128 + r];
         const bool has1 = n > 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(O_FULL, of0 & 1, abort_flag, kWaitNs));
+        ok = __all_sync(0xffffffffu, mbar_wait(O_FULL, of0 & 1, abort_flag, wait_ns));
         if (!ok) break;
         ++of0;
         if (has1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8, of1 & 1, abort_flag, kWaitNs));
+          ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8, of1 & 1, abort_flag, wait_ns));
           if (!ok) break;
           ++of1;
         }
@@ -614,16 +637,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
 }
 
 // --------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 lookup_encode_fn() {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  return nullptr;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_encode_fn();  // initialised once, thread-safe
   return fn;
 }
 
@@ -667,7 +692,8 @@ cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                              "cudaFuncSetAttribute(partials_tc_kernel)");
   if (e != cudaSuccess) return e;
-  TcArgs ta{a, W, npt};
+  const unsigned long long lim = g_wait_limit_ns.load(std::memory_order_relaxed);
+  TcArgs ta{a, W, npt, lim > 0 ? (uint64_t)lim : kDrainNs, g_force_stall.load(std::memory_order_relaxed)};
   e = launch_pdl(partials_tc_kernel<D, kBF16>, dim3(pr.U), dim3(kThreadsTc), (size_t)smem, s, mq, mk, mv, mtk,
                  mtv, ta);
   if (e != cudaSuccess) {
@@ -682,6 +708,11 @@ cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s
 }
 
 }  // namespace
+
+void set_tc_wait_limit(unsigned long long ns, int stall) {
+  g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+  g_force_stall.store(stall != 0 ? 1 : 0, std::memory_order_relaxed);
+}
 
 cudaError_t launch_partials_tc(const PartialArgs& a, bool bf16, int W, int npt, cudaStream_t s) {
   if (bf16) return a.pr.d == 64 ? launch_tc_typed<64, true>(a, W, npt, s) : launch_tc_typed<128, true>(a, W, npt, s);

@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -34,15 +35,16 @@ int device_sms(int* sms) {
   if (tva::check_cuda(cudaGetDevice(&dev), "cudaGetDevice") != cudaSuccess || dev < 0 ||
       dev >= kMaxDevices)
     return -1;
-  static int cache[kMaxDevices] = {0};
-  if (cache[dev] == 0) {
-    int v = 0;
+  // Filled on first use per device; concurrent first calls store the same value.
+  static std::atomic<int> cache[kMaxDevices];
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     if (tva::check_cuda(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev),
                         "cudaDeviceGetAttribute") != cudaSuccess || v <= 0)
       return -1;
-    cache[dev] = v;
+    cache[dev].store(v, std::memory_order_relaxed);
   }
-  *sms = cache[dev];
+  *sms = v;
   return 0;
 }
 
@@ -270,32 +272,29 @@ tva_status tree_verify_attn(const void* q, const void* k_cache, const void* v_ca
   if (st != TVA_OK) return st;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TVA_ERR_CUDA;
-  void* ws = nullptr;
-  int32_t* status = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_owned_mu);
-    OwnedState& o = g_owned[dev];
-    if (o.status == nullptr) {
-      if (cudaMalloc(&o.status, sizeof(int32_t)) != cudaSuccess) return TVA_ERR_CUDA;
-      if (cudaMemset(o.status, 0, sizeof(int32_t)) != cudaSuccess) return TVA_ERR_CUDA;
+  // The lock is held until both kernels are enqueued: another thread that needs a
+  // larger workspace frees the old one only after synchronising the device, and it
+  // cannot do so between this thread's pointer copy and its launches.
+  std::lock_guard<std::mutex> lock(g_owned_mu);
+  OwnedState& o = g_owned[dev];
+  if (o.status == nullptr) {
+    if (cudaMalloc(&o.status, sizeof(int32_t)) != cudaSuccess) return TVA_ERR_CUDA;
+    if (cudaMemset(o.status, 0, sizeof(int32_t)) != cudaSuccess) return TVA_ERR_CUDA;
+  }
+  if (o.ws_bytes < L.total) {
+    if (o.ws != nullptr) {
+      cudaDeviceSynchronize();  // the old buffer may still be in use by queued work
+      cudaFree(o.ws);
+      o.ws = nullptr;
+      o.ws_bytes = 0;
     }
-    if (o.ws_bytes < L.total) {
-      if (o.ws != nullptr) {
-        cudaDeviceSynchronize();  // the old buffer may still be in use by queued work
-        cudaFree(o.ws);
-        o.ws = nullptr;
-        o.ws_bytes = 0;
-      }
-      if (cudaMalloc(&o.ws, L.total) != cudaSuccess) return TVA_ERR_CUDA;
-      o.ws_bytes = L.total;
-    }
-    ws = o.ws;
-    status = o.status;
+    if (cudaMalloc(&o.ws, L.total) != cudaSuccess) return TVA_ERR_CUDA;
+    o.ws_bytes = L.total;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_partials(L, (int)dtype, 0.f, q, k_cache, v_cache, tree_k, tree_v, parent, ws, status, s);
+  st = run_partials(L, (int)dtype, 0.f, q, k_cache, v_cache, tree_k, tree_v, parent, o.ws, o.status, s);
   if (st != TVA_OK) return st;
-  return run_combine(L, (int)dtype, ws, out, lse, status, s);
+  return run_combine(L, (int)dtype, o.ws, out, lse, o.status, s);
 }
 
 tva_status tva_read_device_status(int32_t* host_status, void* stream) {
@@ -315,6 +314,10 @@ tva_status tva_read_device_status(int32_t* host_status, void* stream) {
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return TVA_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return TVA_ERR_CUDA;
   return TVA_OK;
+}
+
+void tva_diag_set_wait_limit(unsigned long long wait_limit_ns, int force_stall) {
+  tva::set_tc_wait_limit(wait_limit_ns, force_stall);
 }
 
 void tva_release(void) {

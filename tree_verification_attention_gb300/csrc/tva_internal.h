@@ -122,6 +122,9 @@ int simt_workers_per_sm();
 cudaError_t launch_partials_simt(const PartialArgs& a, int dtype, cudaStream_t s);
 // bf16 (bf16 = true) or fp16, head_dim 64 or 128; W M-tiles of npt nodes per row group
 cudaError_t launch_partials_tc(const PartialArgs& a, bool bf16, int W, int npt, cudaStream_t s);
+// Main-loop wait limit of the tensor-core partials kernel for later launches (0: the
+// default 2 s) and the test stall (tva_diag_set_wait_limit).
+void set_tc_wait_limit(unsigned long long ns, int stall);
 cudaError_t launch_combine(const CombineArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
 cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);

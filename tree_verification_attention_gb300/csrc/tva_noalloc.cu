@@ -5,8 +5,12 @@
 // engine that owns every device allocation and forbids cudaMalloc (or its own pool)
 // on its execution path, plugins whose per-call interface has no workspace argument,
 // and latency-critical loops that must not risk an allocation.  For them the
-// partials this path needs live in one fixed array in this file, reserved when the
-// library's device code is loaded on a GPU and held until the process exits.
+// partials this path needs live in one fixed array in this file, held on each GPU
+// until the process exits.  The array is reserved when this file's module is loaded
+// on a device: under CUDA's default lazy module loading (this module has no kernels)
+// that is the first cudaGetSymbolAddress below, i.e. the entry point's first call on
+// the device, which then fails with TVA_ERR_CUDA if the device has no 32 MiB left;
+// with CUDA_MODULE_LOADING=EAGER it is when the library's device code is loaded.
 #include <cstdio>
 #include <mutex>
 
