@@ -11,14 +11,12 @@
 // exponentiating (the stable form of the same expression).
 //
 // A warp takes one 32-row block of one row group and CG of its column groups (4
-// columns each); lane t owns row t of the block.  All rows of a row group have the
-// same partials (the same workers covered it), so every lane of the warp runs the same
-// loops and no shuffles are needed; each 16-byte load of a warp reads 512 contiguous
-// bytes of the blocked partial layout (tva_common.cuh).  The kernel is bound by load
-// latency, so a warp issues the loads of up to NB partials at once; CG and NB are picked
-// per launch from the expected number of partials per row group.  It is launched as a
+// columns each); lane t owns row t of the block.  The kernel is bound by load latency,
+// so a warp issues the loads of up to NB partials at once; CG and NB are picked per
+// launch from the expected number of partials per row group.  It is launched as a
 // programmatic dependent of the partials kernel: the walk that locates the row group
 // reads only the caller's cu_* arrays and runs before the wait for the partials.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -30,6 +28,114 @@
 
 namespace tva {
 namespace {
+
+// Writes one merged row piece: out = acc / den (CG column groups from cs * CG) in T, and
+// (for the first column set) lse = (Ms + log2 den) * ln 2 for row r (node `node`) of the
+// row group R.
+template <typename T, int D, int CG>
+__device__ __forceinline__ void store_merged(const Problem& pr, const GroupLoc& R, int node, int r, int cs,
+                                             const float4 (&acc)[CG], float den, float Ms, void* out_v,
+                                             float* lse_out) {
+  const float inv = 1.f / den;
+  const int head = R.g * pr.G + r % pr.G;
+  const size_t orow = ((size_t)(R.s.n0 + node) * pr.Hq + head) * D + (size_t)cs * CG * 4;
+  if constexpr (sizeof(T) == 4) {
+    float4* out = reinterpret_cast<float4*>(static_cast<float*>(out_v) + orow);
+#pragma unroll
+    for (int g = 0; g < CG; ++g)
+      out[g] = make_float4(acc[g].x * inv, acc[g].y * inv, acc[g].z * inv, acc[g].w * inv);
+  } else {
+    uint2* out = reinterpret_cast<uint2*>(static_cast<T*>(out_v) + orow);
+#pragma unroll
+    for (int g = 0; g < CG; ++g) {
+      uint32_t lo, hi;
+      if constexpr (std::is_same<T, __half>::value) {
+        const __half2 l = __floats2half2_rn(acc[g].x * inv, acc[g].y * inv);
+        const __half2 h = __floats2half2_rn(acc[g].z * inv, acc[g].w * inv);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __nv_bfloat162 l = __floats2bfloat162_rn(acc[g].x * inv, acc[g].y * inv);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[g].z * inv, acc[g].w * inv);
+        lo = *reinterpret_cast<const uint32_t*>(&l);
+        hi = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      out[g] = make_uint2(lo, hi);
+    }
+  }
+  if (cs == 0) lse_out[(size_t)(R.s.n0 + node) * pr.Hq + head] = (Ms + log2f(den)) * 0.69314718055994530942f;
+}
+
+// One warp merges one 32-row block (rb) of row group qg for CG of its column groups (4
+// columns each, starting at column group cs * CG); lane t owns padded row rb * 32 + t.
+// The np partials of the row group are in slots slot0 .. slot0 + np - 1 (blocked layout
+// of tva_common.cuh).  Every row of a row group has the same partials (the same workers
+// covered it), so all lanes run the same loops and no shuffles are needed; the loads of
+// up to NB partials are issued in one round.  Lanes whose row is padding return without
+// touching memory; nothing here synchronises the warp.
+template <typename T, int D, int CG, int NB>
+__device__ __forceinline__ void merge_rows(const Problem& pr, const float* o_part, const float* lse_part,
+                                           const GroupLoc& R, size_t slot0, int np, int rb, int cs, int lane,
+                                           void* out_v, float* lse_out) {
+  const int MT = mtile_rows(pr.G);
+  const int W = pr.RG / MT;
+  const int RGP = W * 128;
+  const int pp = rb * 32 + lane;                // padded row of this lane
+  const int mt = pp / 128, r = pp % 128;
+  const int node = (R.mp * W + mt) * (MT / pr.G) + r / pr.G;  // local node id
+  if (!(r < MT && node < R.s.m)) return;
+
+  const float* lse_p = lse_part + slot0 * RGP + pp;
+  const float* o_p = o_part + o_part_offset(slot0, pp, cs * CG, RGP, D);
+  const size_t lstride = (size_t)RGP, ostride = (size_t)RGP * D;
+
+  // Online over rounds of NB partials: each round's LSE and O loads are issued together
+  // (no load waits on another), then the running maximum moves to the round's and the
+  // sums are rescaled - the same result as one maximum over all partials, with
+  // ceil(np / NB) dependent memory rounds.
+  float M = -INFINITY, den = 0.f;
+  float4 acc[CG];
+#pragma unroll
+  for (int g = 0; g < CG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < np; k0 += NB) {
+    float lk[NB];
+    float4 o[NB][CG];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      lk[j] = k0 + j < np ? __ldcg(lse_p + (k0 + j) * lstride) : -INFINITY;
+#pragma unroll
+      for (int g = 0; g < CG; ++g)
+        o[j][g] = k0 + j < np ? __ldcg(reinterpret_cast<const float4*>(o_p + (k0 + j) * ostride + g * 128))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float Mr = M;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) Mr = fmaxf(Mr, lk[j]);
+    const float Ms = (Mr == -INFINITY) ? 0.f : Mr;
+    const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Ms);  // nothing accumulated yet: 0
+    den *= sc;
+#pragma unroll
+    for (int g = 0; g < CG; ++g) {
+      acc[g].x *= sc; acc[g].y *= sc; acc[g].z *= sc; acc[g].w *= sc;
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const float wj = exp2f(lk[j] - Ms);  // exp2(-inf) = 0 for the padding entries
+      den += wj;
+#pragma unroll
+      for (int g = 0; g < CG; ++g) {
+        acc[g].x = fmaf(wj, o[j][g].x, acc[g].x);
+        acc[g].y = fmaf(wj, o[j][g].y, acc[g].y);
+        acc[g].z = fmaf(wj, o[j][g].z, acc[g].z);
+        acc[g].w = fmaf(wj, o[j][g].w, acc[g].w);
+      }
+    }
+    M = Mr;
+  }
+  const float Ms = (M == -INFINITY) ? 0.f : M;
+  store_merged<T, D, CG>(pr, R, node, r, cs, acc, den, Ms, out_v, lse_out);
+}
+
 
 constexpr int kCuCap = 2048;      // ints of shared memory for the staged cu_* arrays
 
@@ -52,10 +158,6 @@ __global__ void __launch_bounds__(32 * WPB) combine_kernel(CombineArgs a) {
   const int cs = (int)(wid % per_group) % NCG;  // column-group set
   const GroupLoc R = locate_group(pr, qg);      // uniform over the warp
   if (!R.found) return;
-  const int pp = rb * 32 + lane;                // padded row of this lane
-  const int mt = pp / 128, r = pp % 128;
-  const int node = (R.mp * W + mt) * (MT / pr.G) + r / pr.G;  // local node id
-  const bool valid = r < MT && node < R.s.m;
   const long long c = chunk_units(pr, R.T);
   const int u0 = (int)(R.start / c);
   const int np = (int)((R.start + R.tiles - 1) / c) - u0 + 1;
@@ -63,90 +165,9 @@ __global__ void __launch_bounds__(32 * WPB) combine_kernel(CombineArgs a) {
     if (lane == 0) set_status(a.status, kStatusInvalidArg);
     return;
   }
-  const size_t slot0 = (size_t)u0 + qg;
-
   ptx::pdl_wait();  // the partials (and every earlier write) are visible after this
   ptx::pdl_launch_dependents();
-  if (!valid) return;  // nothing below synchronises the warp
-
-  const float* lse_p = a.lse_part + slot0 * RGP + pp;
-  const float* o_p = a.o_part + o_part_offset(slot0, pp, cs * CG, RGP, D);
-  const size_t lstride = (size_t)RGP, ostride = (size_t)RGP * D;
-
-  // The first NB partials (LSE and O) are requested in one round; the O rows do not
-  // depend on the maximum.
-  float lk[NB];
-  float4 o[NB][CG];
-#pragma unroll
-  for (int j = 0; j < NB; ++j) {
-    lk[j] = j < np ? __ldg(lse_p + j * lstride) : -INFINITY;
-#pragma unroll
-    for (int g = 0; g < CG; ++g)
-      o[j][g] = j < np ? __ldg(reinterpret_cast<const float4*>(o_p + j * ostride + g * 128))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  float M = -INFINITY;
-#pragma unroll
-  for (int j = 0; j < NB; ++j) M = fmaxf(M, lk[j]);
-  for (int k = NB; k < np; ++k) M = fmaxf(M, __ldg(lse_p + k * lstride));
-  const float Ms = (M == -INFINITY) ? 0.f : M;
-
-  float den = 0.f;
-  float4 acc[CG];
-#pragma unroll
-  for (int g = 0; g < CG; ++g) acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k0 = 0; k0 < np; k0 += NB) {
-    if (k0 > 0) {
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        lk[j] = k0 + j < np ? __ldg(lse_p + (k0 + j) * lstride) : -INFINITY;
-#pragma unroll
-        for (int g = 0; g < CG; ++g)
-          o[j][g] = k0 + j < np ? __ldg(reinterpret_cast<const float4*>(o_p + (k0 + j) * ostride + g * 128))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NB; ++j) {
-      const float wj = k0 + j < np ? exp2f(lk[j] - Ms) : 0.f;
-      den += wj;
-#pragma unroll
-      for (int g = 0; g < CG; ++g) {
-        acc[g].x = fmaf(wj, o[j][g].x, acc[g].x);
-        acc[g].y = fmaf(wj, o[j][g].y, acc[g].y);
-        acc[g].z = fmaf(wj, o[j][g].z, acc[g].z);
-        acc[g].w = fmaf(wj, o[j][g].w, acc[g].w);
-      }
-    }
-  }
-  const float inv = 1.f / den;
-  const int head = R.g * pr.G + r % pr.G;
-  const size_t orow = ((size_t)(R.s.n0 + node) * pr.Hq + head) * D + (size_t)cs * CG * 4;
-  if constexpr (sizeof(T) == 4) {
-    float4* out = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow);
-#pragma unroll
-    for (int g = 0; g < CG; ++g)
-      out[g] = make_float4(acc[g].x * inv, acc[g].y * inv, acc[g].z * inv, acc[g].w * inv);
-  } else {
-    uint2* out = reinterpret_cast<uint2*>(static_cast<T*>(a.out) + orow);
-#pragma unroll
-    for (int g = 0; g < CG; ++g) {
-      uint32_t lo, hi;
-      if constexpr (std::is_same<T, __half>::value) {
-        const __half2 l = __floats2half2_rn(acc[g].x * inv, acc[g].y * inv);
-        const __half2 h = __floats2half2_rn(acc[g].z * inv, acc[g].w * inv);
-        lo = *reinterpret_cast<const uint32_t*>(&l);
-        hi = *reinterpret_cast<const uint32_t*>(&h);
-      } else {
-        const __nv_bfloat162 l = __floats2bfloat162_rn(acc[g].x * inv, acc[g].y * inv);
-        const __nv_bfloat162 h = __floats2bfloat162_rn(acc[g].z * inv, acc[g].w * inv);
-        lo = *reinterpret_cast<const uint32_t*>(&l);
-        hi = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      out[g] = make_uint2(lo, hi);
-    }
-  }
-  if (cs == 0) a.lse[(size_t)(R.s.n0 + node) * pr.Hq + head] = (Ms + log2f(den)) * 0.69314718055994530942f;
+  merge_rows<T, D, CG, NB>(pr, a.o_part, a.lse_part, R, (size_t)u0 + qg, np, rb, cs, lane, a.out, a.lse);
 }
 
 // Row groups the layout provides for (every sequence at its stated maximum size).
@@ -215,7 +236,7 @@ cudaError_t launch_d(const CombineArgs& a, cudaStream_t s) {
   const int np = expected_partials(a.pr);
   if (np <= 6) return launch_typed<T, D, 4, 6>(a, s);
   if (np <= 12) return launch_typed<T, D, 2, 12>(a, s);
-  return launch_typed<T, D, 1, 20>(a, s);
+  return launch_typed<T, D, 2, 20>(a, s);
 }
 
 template <typename T>

@@ -73,6 +73,7 @@ struct Layout {
   long long slots;
 };
 
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Fills the device-visible problem and the workspace layout.  cu_* may be null for
@@ -138,6 +139,21 @@ tva_status run_partials(const Layout& L, int dtype, float softmax_scale, const v
   const cudaError_t e = dtype == TVA_FP32 ? tva::launch_partials_simt(a, dtype, s)
                                           : tva::launch_partials_tc(a, dtype == TVA_BF16, L.W, L.npt, s);
   return e == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
+}
+
+tva_status run_combine(const Layout& L, int dtype, const void* workspace, void* out, float* lse,
+                       int32_t* dev_status, cudaStream_t s);
+
+// The whole attention: the partials launch, then the combine launch (a programmatic
+// dependent of it).
+tva_status run_attention(const Layout& L, int dtype, float softmax_scale, const void* q,
+                         const void* k_cache, const void* v_cache, const void* tree_k,
+                         const void* tree_v, const int32_t* parent, void* workspace,
+                         void* out, float* lse, int32_t* dev_status, cudaStream_t s) {
+  tva_status st = run_partials(L, dtype, softmax_scale, q, k_cache, v_cache, tree_k, tree_v, parent,
+                               workspace, dev_status, s);
+  if (st != TVA_OK) return st;
+  return run_combine(L, dtype, workspace, out, lse, dev_status, s);
 }
 
 tva_status run_combine(const Layout& L, int dtype, const void* workspace, void* out, float* lse,
@@ -251,10 +267,21 @@ tva_status tree_verify_attn_varlen(const tva_params* p, const void* q, const voi
                                    float* lse, void* workspace, size_t workspace_bytes,
                                    int32_t* dev_status, void* stream) {
   if (out == nullptr || lse == nullptr || !aligned16(out)) return TVA_ERR_INVALID_ARG;
-  tva_status st = tree_verify_attn_partials(p, q, k_cache, v_cache, tree_k, tree_v, parent,
-                                            workspace, workspace_bytes, dev_status, stream);
+  if (p == nullptr || p->cu_prefix == nullptr || p->cu_nodes == nullptr || dev_status == nullptr)
+    return TVA_ERR_INVALID_ARG;
+  tva_status st = check_shape(p->batch, p->num_q_heads, p->num_kv_heads, p->head_dim,
+                              (int)p->dtype, p->max_prefix_len, p->max_nodes, p->kv_capacity,
+                              p->node_capacity);
   if (st != TVA_OK) return st;
-  return tree_verify_attn_combine(p, workspace, workspace_bytes, out, lse, dev_status, stream);
+  st = check_io_ptrs(q, k_cache, v_cache, tree_k, tree_v, parent, p->kv_capacity);
+  if (st != TVA_OK) return st;
+  Layout L;
+  st = layout_from_params(p, &L);
+  if (st != TVA_OK) return st;
+  st = check_workspace(L, workspace, workspace_bytes);
+  if (st != TVA_OK) return st;
+  return run_attention(L, (int)p->dtype, p->softmax_scale, q, k_cache, v_cache, tree_k, tree_v, parent,
+                       workspace, out, lse, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 tva_status tree_verify_attn(const void* q, const void* k_cache, const void* v_cache,
@@ -291,10 +318,8 @@ tva_status tree_verify_attn(const void* q, const void* k_cache, const void* v_ca
     if (cudaMalloc(&o.ws, L.total) != cudaSuccess) return TVA_ERR_CUDA;
     o.ws_bytes = L.total;
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_partials(L, (int)dtype, 0.f, q, k_cache, v_cache, tree_k, tree_v, parent, o.ws, o.status, s);
-  if (st != TVA_OK) return st;
-  return run_combine(L, (int)dtype, o.ws, out, lse, o.status, s);
+  return run_attention(L, (int)dtype, 0.f, q, k_cache, v_cache, tree_k, tree_v, parent, o.ws, out, lse,
+                       o.status, static_cast<cudaStream_t>(stream));
 }
 
 tva_status tva_read_device_status(int32_t* host_status, void* stream) {
