@@ -515,6 +515,29 @@ def main():
     torch.cuda.synchronize()
     gdn_ms = float(np.mean([evg[i][0].elapsed_time(evg[i][1]) for i in range(K)]))
     gdn_bytes = sum(x.nbytes for n, x in gc.items() if n not in ("parent", "cu_nodes")) + g_out.numel() * 4
+    # the same shape with bf16 q / k / v / out (fp32 state, gates and arithmetic)
+    gb = {n: (torch.from_numpy(x).to(dev).to(torch.bfloat16) if n in ("q", "k", "v") else torch.from_numpy(x).to(dev))
+          for n, x in workloads.make_gdn_case(batch=1, heads=32, d=128, m=64, tree="best_first", dtype="bf16").items()}
+    gb_out = torch.empty_like(gb["v"])
+
+    def gdn_bf16():
+        api.gdn_tree_verify(gb["cu_nodes"], gb["parent"], gb["q"], gb["k"], gb["v"], gb["beta"], gb["alpha"],
+                            gb["S0"], out=gb_out, max_nodes=64, dev_status=status)
+
+    for _ in range(args.warmup):
+        gdn_bf16()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(20e6))
+    for i in range(K):
+        flush.fill_((i + 13) & 0xFF)
+        torch.cuda._sleep(int(dither.integers(0, 8192)))
+        evg[i][0].record(stream)
+        gdn_bf16()
+        evg[i][1].record(stream)
+    torch.cuda.synchronize()
+    gdn16_ms = float(np.mean([evg[i][0].elapsed_time(evg[i][1]) for i in range(K)]))
+    gdn16_bytes = sum(x.numel() * x.element_size() for n, x in gb.items() if n not in ("parent", "cu_nodes")) + \
+        gb_out.numel() * 2
 
     # ---- end to end through the public API from pinned host buffers
     pinned = {k: v.pin_memory() for k, v in host.items()}
@@ -654,6 +677,10 @@ def main():
         "chain_sampling": {"workload": "B=8 chains, gamma=8, V=128256, fp32 p/q", "us_per_launch": sample_ms * 1e3,
                            "bytes": sample_bytes, "gbs": sample_bytes / (sample_ms * 1e-3) / 1e9,
                            "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
+        "gdn_tree_bf16": {"workload": "B=1, H=32, d=128, 64-node best-first tree, bf16 q/k/v/out, fp32 state",
+                          "us_per_launch": gdn16_ms * 1e3, "bytes": gdn16_bytes,
+                          "gbs": gdn16_bytes / (gdn16_ms * 1e-3) / 1e9,
+                          "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
         "gdn_tree": {"workload": "B=1, H=32, d=128, 64-node best-first tree, fp32", "us_per_launch": gdn_ms * 1e3,
                      "bytes": gdn_bytes, "gbs": gdn_bytes / (gdn_ms * 1e-3) / 1e9,
                      "timed": f"{K} launches alone (not in the step), L2 flushed before each"},

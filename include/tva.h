@@ -268,19 +268,23 @@ tva_status verify_chain_sampling(int batch, int vocab, int max_draft, long long 
  * pairs, solved by forward substitution, and the state itself is not updated (its
  * commit waits for the accepted branch).  Node i's output is o_i = S_i^T q_i with S_i
  * the state after running the update along the root-to-i path from S0.  The pages give
- * no interface.  All pointers are device pointers, fp32, row-major:
+ * no interface.  All pointers are device pointers, row-major:
  *   batch, num_heads (H), head_dim (d: 64 or 128)
+ *   dtype         type of q, k, v and out: TVA_FP32, or TVA_BF16 (the precision the page's
+ *                 measurements use); beta, alpha and S0 are always fp32, and every
+ *                 arithmetic step is fp32 (bf16 inputs widened, the output rounded once)
  *   node_capacity rows of q, k, v, out [node_capacity, H, d] and beta, alpha [node_capacity, H]
  *   max_nodes     bound on every m_b (<= 128)
  *   cu_nodes      [B+1], parent [N] local ids in [-1, i) (as for the attention)
- *   S0            [B, H, d, d] committed state at each sequence's prefix end (rows: keys)
+ *   S0            [B, H, d, d] fp32 committed state at each sequence's prefix end (rows: keys)
  *   out           [N, H, d]
- * q, k, v, S0 and out are 16-byte aligned.  A sequence outside the bounds is skipped with TVA_ERR_INVALID_ARG, a non-topological
+ * q, k, v, S0 and out are 16-byte aligned.  Any other dtype returns TVA_ERR_UNSUPPORTED.
+ * A sequence outside the bounds is skipped with TVA_ERR_INVALID_ARG, a non-topological
  * parent array with TVA_ERR_BAD_TREE, in *dev_status. */
-tva_status gdn_tree_verify(int batch, int num_heads, int head_dim, int node_capacity, int max_nodes,
-                           const int32_t* cu_nodes, const int32_t* parent, const float* q, const float* k,
-                           const float* v, const float* beta, const float* alpha, const float* S0, float* out,
-                           int32_t* dev_status, void* stream);
+tva_status gdn_tree_verify(int batch, int num_heads, int head_dim, tva_dtype dtype, int node_capacity,
+                           int max_nodes, const int32_t* cu_nodes, const int32_t* parent, const void* q,
+                           const void* k, const void* v, const float* beta, const float* alpha, const float* S0,
+                           void* out, int32_t* dev_status, void* stream);
 
 /* Description of the last host-side CUDA or driver failure seen by this thread
  * (the call that failed and its error string), "" if none.  Thread-local storage,

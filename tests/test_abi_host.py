@@ -45,6 +45,13 @@ def test_every_declared_symbol_is_exported(lib):
     assert os.path.dirname(build.LIB_PATH).endswith("tree_verification_attention_gb300")
 
 
+def test_checked_build_exports_the_same_entry_points(lib):
+    """libtva_checked.so (device-side index checks) is a drop-in for libtva.so."""
+    checked = ctypes.CDLL(build.build(checked=True))
+    missing = [n for n in _declared_functions() if not hasattr(checked, n)]
+    assert not missing, missing
+
+
 def test_status_strings(lib):
     assert api.status_string(0) == "TVA_OK"
     assert api.status_string(3) == "TVA_ERR_BAD_TREE"

@@ -49,11 +49,13 @@ _SZ = ctypes.c_size_t
 
 
 def load_library(path: str | None = None):
-    """Load libtva.so (built by ``build.build()``); raises if it is absent."""
+    """Load libtva.so (built by ``build.build()``); raises if it is absent.  The
+    environment variable TVA_LIBRARY selects another build of the same library (for
+    example libtva_checked.so, the index-checked variant)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or _build.LIB_PATH
+    path = path or os.environ.get("TVA_LIBRARY") or _build.LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: run tree_verification_attention_gb300.build.build() "
                            "(or __graft_entry__.build()) first; there is no fallback path")
@@ -74,7 +76,7 @@ def load_library(path: str | None = None):
                                     _P, _P]),
         "verify_chain_sampling": (_I, [_I, _I, _I, ctypes.c_longlong, ctypes.c_longlong, _P, _P, _P, _P, _P, _P,
                                        _P, _P, _P, _P]),
-        "gdn_tree_verify": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "gdn_tree_verify": (_I, [_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "tva_status_string": (ctypes.c_char_p, [_I]),
         "tva_last_error": (ctypes.c_char_p, []),
     }
@@ -324,11 +326,16 @@ def verify_chain_sampling(cu_draft, p, q, draft_tok, u_accept, u_sample, max_dra
 
 def gdn_tree_verify(cu_nodes, parent, q, k, v, beta, alpha, S0, out=None, max_nodes=None, dev_status=None,
                     stream=None):
-    """Gated DeltaNet tree verification.  q, k, v [N, H, d]; beta, alpha [N, H]; S0 [B, H, d, d];
-    all float32 CUDA tensors.  Returns out [N, H, d] float32."""
+    """Gated DeltaNet tree verification.  q, k, v [N, H, d] float32 or bfloat16 (all three
+    alike); beta, alpha [N, H] and S0 [B, H, d, d] float32; CUDA tensors.  Returns out
+    [N, H, d] in q's dtype."""
     for name, t in (("cu_nodes", cu_nodes), ("parent", parent)):
         _dev(t, name, torch.int32)
-    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("alpha", alpha), ("S0", S0)):
+    if q.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"unsupported dtype {q.dtype}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _dev(t, name, q.dtype)
+    for name, t in (("beta", beta), ("alpha", alpha), ("S0", S0)):
         _dev(t, name, torch.float32)
     B = cu_nodes.numel() - 1
     N, H, d = q.shape
@@ -338,9 +345,9 @@ def gdn_tree_verify(cu_nodes, parent, q, k, v, beta, alpha, S0, out=None, max_no
         out = torch.empty_like(v)
     if dev_status is None:
         dev_status = torch.zeros(1, dtype=torch.int32, device=q.device)
-    code = load_library().gdn_tree_verify(B, H, d, N, max(1, int(max_nodes)), _ptr(cu_nodes), _ptr(parent),
-                                          _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha), _ptr(S0),
-                                          _ptr(out), _ptr(dev_status), _stream(stream))
+    code = load_library().gdn_tree_verify(B, H, d, DTYPES[q.dtype], N, max(1, int(max_nodes)), _ptr(cu_nodes),
+                                          _ptr(parent), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(alpha),
+                                          _ptr(S0), _ptr(out), _ptr(dev_status), _stream(stream))
     _check(code, "gdn_tree_verify")
     return out
 

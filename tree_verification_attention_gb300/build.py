@@ -19,6 +19,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libtva.so")
+# The checked build: the same sources with -DTVA_CHECKED (device-side index checks that
+# record TVA_ERR_INVALID_ARG instead of touching memory out of bounds; see tva_common.cuh).
+CHECKED_BUILD_DIR = os.path.join(PKG, "_build_checked")
+CHECKED_LIB_PATH = os.path.join(PKG, "libtva_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
@@ -49,20 +53,23 @@ def _stamp() -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link; return the path of libtva.so."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    stamp = _stamp() + ("|" + " ".join(extra_flags) if extra_flags else "")
-    stamp_path = os.path.join(BUILD_DIR, "stamp")
-    if not force and os.path.exists(LIB_PATH) and os.path.exists(stamp_path):
+def build(force: bool = False, verbose: bool = False, extra_flags=None, checked: bool = False) -> str:
+    """Compile and link; return the path of libtva.so (libtva_checked.so with checked=True)."""
+    build_dir = CHECKED_BUILD_DIR if checked else BUILD_DIR
+    lib_path = CHECKED_LIB_PATH if checked else LIB_PATH
+    extra = list(extra_flags or []) + (["-DTVA_CHECKED"] if checked else [])
+    os.makedirs(build_dir, exist_ok=True)
+    stamp = _stamp() + ("|" + " ".join(extra) if extra else "")
+    stamp_path = os.path.join(build_dir, "stamp")
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_path):
         with open(stamp_path) as f:
             if f.read() == stamp:
-                return LIB_PATH
+                return lib_path
     nvcc = _nvcc()
-    flags = CFLAGS + list(extra_flags or [])
+    flags = CFLAGS + extra
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -74,16 +81,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs + ["-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    os.replace(tmp, lib_path)
     with open(stamp_path, "w") as f:
         f.write(stamp)
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":
     print(build(verbose=True))
+    print(build(verbose=True, checked=True))

@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kWarps * 32) accept_kernel(AcceptArgs a) {
   if (lane == 0) {
     int j = best;
     for (int pos = depth - 1; pos >= 0; --pos) {
+      if (!TVA_CHECK(pos < m && j >= 0 && j < m, a.status)) break;
       a.accept_path[n0 + pos] = j;
       j = s_par[w][j];
     }

@@ -35,9 +35,10 @@ namespace {
 template <typename T, int D, int CG>
 __device__ __forceinline__ void store_merged(const Problem& pr, const GroupLoc& R, int node, int r, int cs,
                                              const float4 (&acc)[CG], float den, float Ms, void* out_v,
-                                             float* lse_out) {
+                                             float* lse_out, int32_t* status) {
   const float inv = 1.f / den;
   const int head = R.g * pr.G + r % pr.G;
+  if (!TVA_CHECK(R.s.n0 + node < pr.node_capacity && head < pr.Hq && (cs + 1) * CG * 4 <= D, status)) return;
   const size_t orow = ((size_t)(R.s.n0 + node) * pr.Hq + head) * D + (size_t)cs * CG * 4;
   if constexpr (sizeof(T) == 4) {
     float4* out = reinterpret_cast<float4*>(static_cast<float*>(out_v) + orow);
@@ -76,7 +77,7 @@ __device__ __forceinline__ void store_merged(const Problem& pr, const GroupLoc& 
 template <typename T, int D, int CG, int NB>
 __device__ __forceinline__ void merge_rows(const Problem& pr, const float* o_part, const float* lse_part,
                                            const GroupLoc& R, size_t slot0, int np, int rb, int cs, int lane,
-                                           void* out_v, float* lse_out) {
+                                           void* out_v, float* lse_out, int32_t* status) {
   const int MT = mtile_rows(pr.G);
   const int W = pr.RG / MT;
   const int RGP = W * 128;
@@ -133,7 +134,7 @@ __device__ __forceinline__ void merge_rows(const Problem& pr, const float* o_par
     M = Mr;
   }
   const float Ms = (M == -INFINITY) ? 0.f : M;
-  store_merged<T, D, CG>(pr, R, node, r, cs, acc, den, Ms, out_v, lse_out);
+  store_merged<T, D, CG>(pr, R, node, r, cs, acc, den, Ms, out_v, lse_out, status);
 }
 
 
@@ -167,7 +168,8 @@ __global__ void __launch_bounds__(32 * WPB) combine_kernel(CombineArgs a) {
   }
   ptx::pdl_wait();  // the partials (and every earlier write) are visible after this
   ptx::pdl_launch_dependents();
-  merge_rows<T, D, CG, NB>(pr, a.o_part, a.lse_part, R, (size_t)u0 + qg, np, rb, cs, lane, a.out, a.lse);
+  merge_rows<T, D, CG, NB>(pr, a.o_part, a.lse_part, R, (size_t)u0 + qg, np, rb, cs, lane, a.out, a.lse,
+                           a.status);
 }
 
 // Row groups the layout provides for (every sequence at its stated maximum size).

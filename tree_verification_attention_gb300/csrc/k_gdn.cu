@@ -13,7 +13,9 @@
 // and the state itself is never updated here (the commit waits for the accepted branch).
 // The ratios gamma_i / gamma_j are products of alpha walked up from i to j (no division).
 //
-// One CTA (1024 threads) per (sequence, head), fp32 throughout:
+// One CTA (1024 threads) per (sequence, head).  q, k, v and the output are fp32 or bf16
+// (T); beta, alpha and the state are fp32, and all arithmetic is fp32 (bf16 inputs are
+// widened as they are staged; the output is rounded to T once):
 //   1. parents -> depth and path product (a thread per node), list offsets (a scan) and the
 //      depth-level order; K, Q and this CTA's columns of S_0 staged in shared memory;
 //   2. interaction values over ancestor pairs only: X (k.k) and Y (q.k), one pair per thread;
@@ -22,11 +24,30 @@
 //      to shared memory (over Q), gamma_i Q S_0 stays in registers;
 //   4. forward substitution one depth level at a time (nodes of a level are independent);
 //   5. the output sum over each node's ancestors-or-self.
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
 #include "tc_ptx.cuh"
 #include "tva_internal.h"
 
 namespace tva {
 namespace {
+
+__device__ __forceinline__ float gdn_load(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float gdn_load(const __nv_bfloat16* p) { return __bfloat162float(__ldg(p)); }
+// four consecutive elements (16-byte aligned for float, 8-byte for bf16)
+__device__ __forceinline__ float4 gdn_load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 gdn_load4(const __nv_bfloat16* p) {
+  const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+  return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+}
+__device__ __forceinline__ void gdn_store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void gdn_store4(__nv_bfloat16* p, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  *reinterpret_cast<uint2*>(p) =
+      make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+}
 
 constexpr int kThreadsGdn = 1024;
 constexpr int kMaxPairs = kMaxNodes * (kMaxNodes + 1) / 2;   // a chain of kMaxNodes
@@ -48,7 +69,7 @@ struct GdnSmem {
   static constexpr size_t kBytes = (size_t)kFloats * 4 + (size_t)kInts * 4 + (size_t)kMaxNodes * 4 * 3;
 };
 
-template <int D>
+template <int D, typename T>
 __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   using SM = GdnSmem<D>;
   constexpr int CS = D / kCols;                // CTAs per (sequence, head)
@@ -95,8 +116,8 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   for (int e = tid; e < m * D; e += kThreadsGdn) {
     const int i = e / D, r = e % D;
     const size_t src = (size_t)(n0 + i) * hs + (size_t)h * D + r;
-    sK[i * SM::kKPitch + r] = __ldg(a.k + src);
-    sQ[i * SM::kQPitch + r] = __ldg(a.q + src);
+    sK[i * SM::kKPitch + r] = gdn_load(static_cast<const T*>(a.k) + src);
+    sQ[i * SM::kQPitch + r] = gdn_load(static_cast<const T*>(a.q) + src);
   }
   const float* S0 = a.S0 + ((size_t)b * a.H + h) * D * D + c0;
   for (int e = tid; e < D * (kCols / 4); e += kThreadsGdn) {
@@ -219,8 +240,7 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   for (int t = 0; t < RPT; ++t) {
     const int i = rg + t * RGS;
     if (i < m) {
-      const float4 vv =
-          __ldg(reinterpret_cast<const float4*>(a.v + (size_t)(n0 + i) * hs + (size_t)h * D + c0) + cg);
+      const float4 vv = gdn_load4(static_cast<const T*>(a.v) + (size_t)(n0 + i) * hs + (size_t)h * D + c0 + 4 * cg);
       const float bt = s_beta[i], gm = s_gam[i];
       *reinterpret_cast<float4*>(sW + i * SM::kWPitch + 4 * cg) =
           make_float4(bt * (vv.x - gm * ks[t].x), bt * (vv.y - gm * ks[t].y), bt * (vv.z - gm * ks[t].z),
@@ -261,19 +281,19 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
         acc.z = fmaf(y, w.z, acc.z); acc.w = fmaf(y, w.w, acc.w);
         j = s_par[j];
       }
-      *(reinterpret_cast<float4*>(a.o + (size_t)(n0 + i) * hs + (size_t)h * D + c0) + cg) = acc;
+      gdn_store4(static_cast<T*>(a.o) + (size_t)(n0 + i) * hs + (size_t)h * D + c0 + 4 * cg, acc);
     }
   }
 }
 
-template <int D>
+template <int D, typename T>
 cudaError_t launch_gdn_typed(const GdnArgs& a, cudaStream_t s) {
   constexpr size_t smem = GdnSmem<D>::kBytes;
-  cudaError_t e = check_cuda(cudaFuncSetAttribute(gdn_tree_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = check_cuda(cudaFuncSetAttribute(gdn_tree_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   (int)smem),
                              "cudaFuncSetAttribute(gdn_tree_kernel)");
   if (e != cudaSuccess) return e;
-  return check_cuda(launch_pdl(gdn_tree_kernel<D>, dim3((unsigned)(a.B * a.H * (D / kCols))), dim3(kThreadsGdn),
+  return check_cuda(launch_pdl(gdn_tree_kernel<D, T>, dim3((unsigned)(a.B * a.H * (D / kCols))), dim3(kThreadsGdn),
                                smem, s, a),
                     "launch gdn_tree_kernel");
 }
@@ -281,7 +301,8 @@ cudaError_t launch_gdn_typed(const GdnArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_gdn(const GdnArgs& a, cudaStream_t s) {
-  return a.d == 64 ? launch_gdn_typed<64>(a, s) : launch_gdn_typed<128>(a, s);
+  if (a.bf16) return a.d == 64 ? launch_gdn_typed<64, __nv_bfloat16>(a, s) : launch_gdn_typed<128, __nv_bfloat16>(a, s);
+  return a.d == 64 ? launch_gdn_typed<64, float>(a, s) : launch_gdn_typed<128, float>(a, s);
 }
 
 }  // namespace tva

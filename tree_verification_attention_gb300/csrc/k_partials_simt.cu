@@ -211,12 +211,14 @@ __global__ void __launch_bounds__(kThreads, 3) partials_simt_kernel(PartialArgs 
         const int rr = my_row - row_begin, MT = mtile_rows(pr.G);
         const int pp = rr / MT * 128 + rr % MT;  // padded row (see o_part_offset)
         const int RGP = padded_group_rows(pr.RG, pr.G);
+        if (TVA_CHECK(pp < RGP, a.status)) {
 #pragma unroll
-        for (int k = 0; k < D / 8; ++k) {
-          const int c = kg + 8 * k;
-          a.o_part[o_part_offset(slot, pp, c >> 2, RGP, D) + (c & 3)] = o[k] * inv;
+          for (int k = 0; k < D / 8; ++k) {
+            const int c = kg + 8 * k;
+            a.o_part[o_part_offset(slot, pp, c >> 2, RGP, D) + (c & 3)] = o[k] * inv;
+          }
+          if (kg == 0) a.lse_part[(size_t)slot * RGP + pp] = m_run + log2f(l_run);
         }
-        if (kg == 0) a.lse_part[(size_t)slot * RGP + pp] = m_run + log2f(l_run);
       }
     }
     t = seg_end;

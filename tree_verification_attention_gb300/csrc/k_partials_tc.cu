@@ -239,10 +239,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         const int qb = q_buffer(W, sg), quse = q_use(W, sg);
         if (quse > 0 && !warp_wait(Q_EMPTY + 8 * qb, (quse - 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
         mbar_expect_tx_elect(Q_FULL + 8 * qb, (uint32_t)W * C::kHalves * q_box_bytes);
-        for (int mt = 0; mt < W; ++mt)
+        for (int mt = 0; mt < W; ++mt) {
+          // an M-tile starts at a node of its own sequence, or lies wholly past the sequence's
+          // nodes (padding rows: loaded - zeros past the tensor's end - but never written)
+          int qrow = L.s.n0 + (L.mp * W + mt) * npt;
+          if (!TVA_CHECK(qrow >= L.s.n0 && L.g >= 0 && L.g < pr.Hkv, a.status)) qrow = 0;
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d_elect(q_s + ((qb + mt) * C::kHalves + h) * kHalfBytes, &tm_q, 64 * h, L.g * G,
-                        L.s.n0 + (L.mp * W + mt) * npt, Q_FULL + 8 * qb);
+            tma_load_3d_elect(q_s + ((qb + mt) * C::kHalves + h) * kHalfBytes, &tm_q, 64 * h, L.g * G, qrow,
+                              Q_FULL + 8 * qb);
+        }
         const int n = S.n;
         auto load = [&](int k, bool is_v) -> bool {
           const int stage = ring % C::kStages, use = ring / C::kStages;
@@ -251,7 +256,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           const int tile = S.tile0 + k;
           const bool tree = tile == 0;
           const CUtensorMap* m = tree ? (is_v ? &tm_tv : &tm_tk) : (is_v ? &tm_v : &tm_k);
-          const int z = tree ? L.s.n0 : L.s.p0 + (tile - 1) * kKeyTile;
+          int z = tree ? L.s.n0 : L.s.p0 + (tile - 1) * kKeyTile;
+          // a tile starts inside its sequence's rows (loads past a tensor's end read zeros)
+          if (!TVA_CHECK(z >= 0 && (tree ? z < pr.node_capacity && L.s.m > 0
+                                         : z < L.s.p0 + L.s.P && z < pr.kv_capacity), a.status))
+            z = 0;
           mbar_expect_tx_elect(KV_FULL + 8 * stage, C::kTileBytes);
           for (int h = 0; h < C::kHalves; ++h)
             tma_load_3d_hint_elect(kv_s + stage * C::kTileBytes + h * kHalfBytes, m, 64 * h, L.g, z,
@@ -552,6 +561,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         row_ok = false;
       }
       const int pp = mt * 128 + r;  // padded row: lane = row within a 32-row block
+      if (row_ok && !TVA_CHECK(pp < W * 128 && node >= 0 && node < L.s.m, a.status)) row_ok = false;
       float* oblk = a.o_part + o_part_offset(slot, pp, 0, W * 128, D);
       if (W == 2) {
         ok = __all_sync(0xffffffffu, mbar_wait(O_FULL + 8 * w, (w == 0 ? of0 : of1) & 1, abort_flag, wait_ns));

@@ -58,6 +58,22 @@ __device__ __forceinline__ void set_status(int32_t* st, int code) {
   if (st != nullptr) atomicCAS(reinterpret_cast<int*>(st), 0, code);
 }
 
+// Checked build (compiled with -DTVA_CHECKED; libtva_checked.so).  TVA_CHECK(cond, st)
+// guards an index the kernels compute themselves - a TMA tile coordinate, a partial slot,
+// an output row, a position on an accepted path - that a consistent schedule keeps in
+// bounds.  In the checked build a failed check records TVA_ERR_INVALID_ARG in *st and
+// evaluates to false, so the access is skipped (or its coordinate clamped); nothing
+// traps.  In the normal build the checks compile to `true`.
+__device__ __forceinline__ bool checked_ok(bool cond, int32_t* st) {
+  if (!cond) set_status(st, kStatusInvalidArg);
+  return cond;
+}
+#ifdef TVA_CHECKED
+#define TVA_CHECK(cond, st) (::tva::checked_ok((cond), (st)))
+#else
+#define TVA_CHECK(cond, st) (true)
+#endif
+
 __device__ __forceinline__ SeqInfo seq_info(const Problem& pr, int b) {
   SeqInfo s;
   if (pr.cu_prefix == nullptr) {

@@ -425,18 +425,20 @@ tva_status verify_chain_sampling(int batch, int vocab, int max_draft, long long 
   return tva::launch_sampling(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
 }
 
-tva_status gdn_tree_verify(int batch, int num_heads, int head_dim, int node_capacity, int max_nodes,
-                           const int32_t* cu_nodes, const int32_t* parent, const float* q, const float* k,
-                           const float* v, const float* beta, const float* alpha, const float* S0, float* out,
-                           int32_t* dev_status, void* stream) {
+tva_status gdn_tree_verify(int batch, int num_heads, int head_dim, tva_dtype dtype, int node_capacity,
+                           int max_nodes, const int32_t* cu_nodes, const int32_t* parent, const void* q,
+                           const void* k, const void* v, const float* beta, const float* alpha, const float* S0,
+                           void* out, int32_t* dev_status, void* stream) {
   if (batch < 1 || num_heads < 1 || (head_dim != 64 && head_dim != 128) || node_capacity < 0 || max_nodes < 1 ||
       max_nodes > tva::kMaxNodes || !cu_nodes || !parent || !q || !k || !v || !beta || !alpha || !S0 || !out ||
       !dev_status)
     return TVA_ERR_INVALID_ARG;
+  if (dtype != TVA_FP32 && dtype != TVA_BF16) return TVA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S0) || !aligned16(out))
     return TVA_ERR_INVALID_ARG;
   tva::GdnArgs a;
   a.B = batch; a.H = num_heads; a.d = head_dim; a.max_nodes = max_nodes; a.node_capacity = node_capacity;
+  a.bf16 = dtype == TVA_BF16 ? 1 : 0;
   a.cu_nodes = cu_nodes; a.parent = parent; a.q = q; a.k = k; a.v = v; a.beta = beta; a.alpha = alpha;
   a.S0 = S0; a.o = out; a.status = dev_status;
   return tva::launch_gdn(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;

@@ -81,15 +81,16 @@ struct SamplingArgs {
 
 struct GdnArgs {
   int B, H, d, max_nodes, node_capacity;
+  int bf16;                 // q, k, v and o: bf16 (1) or fp32 (0)
   const int32_t* cu_nodes;
   const int32_t* parent;
-  const float* q;
-  const float* k;
-  const float* v;
+  const void* q;
+  const void* k;
+  const void* v;
   const float* beta;
   const float* alpha;
   const float* S0;
-  float* o;
+  void* o;
   int32_t* status;
 };
 

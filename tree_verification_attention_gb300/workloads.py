@@ -417,8 +417,10 @@ def make_chain_sampling_case(batch: int = 8, gamma: int = 8, vocab: int = 128256
 
 
 def make_gdn_case(batch: int = 1, heads: int = 32, d: int = 128, m: int = 64, tree: str = "best_first",
-                  seed: int = 3003, parents=None):
-    """Synthetic inputs for Gated DeltaNet tree verification (fp32 throughout).
+                  seed: int = 3003, parents=None, dtype: str = "fp32"):
+    """Synthetic inputs for Gated DeltaNet tree verification (fp32, or with dtype="bf16"
+    q, k and v rounded once to bfloat16 - returned as float32 arrays holding exactly the
+    bfloat16 values, so the same arrays feed the oracle and a bf16 device copy).
 
     q and k are L2-normalised per (node, head) as Gated DeltaNet layers normalise them;
     v ~ N(0, 1); beta = sigmoid(z) in (0, 1); alpha = exp(-0.1 softplus(z)) (decays
@@ -456,4 +458,8 @@ def make_gdn_case(batch: int = 1, heads: int = 32, d: int = 128, m: int = 64, tr
     vs = rng.standard_normal((batch, heads, 32, d)).astype(np.float32)
     S0 = (0.25 * np.einsum("bhtk,bhtv->bhkv", ks, vs)).astype(np.float32)
     parent = np.concatenate(parents).astype(np.int32) if parents else np.zeros(0, np.int32)
+    if dtype == "bf16":
+        q, k, v = (bits_to_f64(bf16_round_bits(x)).astype(np.float32) for x in (q, k, v))
+    elif dtype != "fp32":
+        raise ValueError(dtype)
     return dict(q=q, k=k, v=v, beta=beta, alpha=alpha, S0=S0, parent=parent, cu_nodes=cu_nodes)
