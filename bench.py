@@ -78,7 +78,7 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-PARTIALS_SOURCES = ("k_partials_tc.cu", "tc_ptx.cuh", "tva_common.cuh", "tva_internal.h")
+PARTIALS_SOURCES = ("k_partials_tc.cu", "tc_pipeline.cuh", "tc_ptx.cuh", "tva_common.cuh", "tva_internal.h")
 
 
 def kernel_source_hash():
@@ -433,6 +433,20 @@ def main():
     # The attention alone (partials + combine), and the dominant kernel alone (partials).
     att_ms, att_iso = timed(lambda: attn(d), 3)
     k1, k1_iso = timed(lambda: step(d), 7)
+    # The CTA-pair partials kernel (a diagnostic selection of the library: cta_group::2,
+    # M = 256, each SM loading half of every K/V tile), timed the same way for comparison;
+    # it applies to two-M-tile row groups at head_dim 128 in 16-bit types.
+    pair_applies = (w.dtype != "fp32" and w.head_dim == 128
+                    and int(w.tree_sizes.max()) * (w.num_q_heads // w.num_kv_heads) > 128)
+    pair_ms = pair_iso = None
+    if pair_applies:
+        api.diag_use_cta_pair(True)
+        try:
+            for _ in range(args.warmup):
+                step(d)
+            pair_ms, pair_iso = timed(lambda: step(d), 11)
+        finally:
+            api.diag_use_cta_pair(False)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -666,6 +680,13 @@ def main():
             "step_roofline_frac": roof_s / (ms_iso * 1e-3), "attention_roofline_frac": roof_s / (att_iso * 1e-3),
             "timed": f"{K} calls one at a time, each between its own events after a random GPU sleep"},
         "roofline": roofline_obj,
+        "cta_pair_partials": None if pair_ms is None else {
+            "kernel": "partials on CTA pairs (cta_group::2, M = 256; tva_diag_use_cta_pair), not the default",
+            "us_per_launch": pair_ms * 1e3,
+            "us_per_launch_isolated": None if pair_iso is None else pair_iso * 1e3,
+            "frac": ((flops / (pair_ms * 1e-3) / 1e12) / tc_peak if tensor_bound
+                     else (k1_bytes / (pair_ms * 1e-3) / 1e9) / hbm_peak),
+            "timed": "as roofline"},
         "cpu_baseline": cpu,
         "e2e": {"value": world * N / (e2e_ms * 1e-3), "unit": "nodes/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
@@ -686,7 +707,7 @@ def main():
                      "timed": f"{K} launches alone (not in the step), L2 flushed before each"},
         # this library's kernels in the timed region: steps (3 each), attention (2), partials (1);
         # with streamed inputs each is timed back to back and once more one call at a time
-        "gpu_launches": (12 if stream_l2 else 6) * K,
+        "gpu_launches": ((12 if stream_l2 else 6) + (0 if pair_ms is None else (2 if stream_l2 else 1))) * K,
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -181,6 +181,18 @@ void tva_release(void);
  * launch are unspecified.  Call tva_diag_set_wait_limit(0, 0) to return to normal. */
 void tva_diag_set_wait_limit(unsigned long long wait_limit_ns, int force_stall);
 
+/* Diagnostics, for comparing two designs of the attention partials; not for production
+ * use.  With enable non-zero, later calls whose problems have row groups of two M-tiles
+ * (max_nodes * G > 128) at head_dim 128 in bf16 / fp16 run the CTA-pair partials kernel
+ * (LongSpec's split key-value partials, "Fast Tree Attention", computed by two SMs per
+ * worker: one M = 256 tensor-core MMA, cta_group::2, covers both M-tiles, each SM loads
+ * half of every K/V tile) instead of the default one-SM-per-worker kernel.  Results
+ * agree with the default within rounding-order differences (the row sums are added in
+ * another order).  The pair kernel runs half as many workers, so a workspace sized while
+ * it is selected can be too small for the default kernel (TVA_ERR_WORKSPACE).  Process-
+ * wide; call with 0 to return to the default. */
+void tva_diag_use_cta_pair(int enable);
+
 /* Greedy longest accepted path per sequence ("Faster decoding", greedy contract).
  *   cu_nodes      [B+1] device, as in tva_params
  *   parent        [N] int32 local parent ids; draft_tok [N] int32 draft tokens

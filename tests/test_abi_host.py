@@ -35,7 +35,7 @@ def test_header_declares_the_expected_entry_points():
     for n in ("tree_verify_attn_varlen", "tree_verify_attn", "accept_longest_path",
               "tva_workspace_size", "tree_verify_attn_partials", "tree_verify_attn_combine",
               "tva_status_string", "tva_release", "tva_read_device_status", "tva_num_workers",
-              "commit_accepted_kv", "verify_chain_sampling", "gdn_tree_verify", "tva_diag_set_wait_limit"):
+              "commit_accepted_kv", "verify_chain_sampling", "gdn_tree_verify", "tva_diag_set_wait_limit", "tva_diag_use_cta_pair"):
         assert n in names
 
 

@@ -17,7 +17,7 @@ from . import build as _build
 __all__ = [
     "TvaError", "Params", "load_library", "workspace_size", "num_workers",
     "tree_verify_attn_varlen", "tree_verify_attn_partials", "tree_verify_attn_combine",
-    "tree_verify_attn", "read_device_status", "release", "diag_set_wait_limit", "accept_longest_path",
+    "tree_verify_attn", "read_device_status", "release", "diag_set_wait_limit", "diag_use_cta_pair", "accept_longest_path",
     "status_string", "STATUS",
 ]
 
@@ -71,6 +71,7 @@ def load_library(path: str | None = None):
         "tva_read_device_status": (_I, [ctypes.POINTER(ctypes.c_int32), _P]),
         "tva_release": (None, []),
         "tva_diag_set_wait_limit": (None, [ctypes.c_ulonglong, _I]),
+        "tva_diag_use_cta_pair": (None, [_I]),
         "accept_longest_path": (_I, [_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "commit_accepted_kv": (_I, [_I, _I, _I, _I, _I, _I, ctypes.c_longlong, _P, _P, _P, _P, _P, _P, _P, _P,
                                     _P, _P]),
@@ -236,6 +237,13 @@ def diag_set_wait_limit(wait_limit_ns: int = 0, force_stall: bool = False):
     wait limit of the tensor-core partials kernel in ns (0 = default 2 s) and, with
     ``force_stall``, a wait that nothing completes.  Call with no arguments to reset."""
     load_library().tva_diag_set_wait_limit(int(wait_limit_ns), 1 if force_stall else 0)
+
+
+def diag_use_cta_pair(enable: bool = False):
+    """Diagnostics (tva_diag_use_cta_pair): select the CTA-pair partials kernel
+    (cta_group::2, M = 256) for later calls where it applies; call with no argument to
+    return to the default one-SM-per-worker kernel."""
+    load_library().tva_diag_use_cta_pair(1 if enable else 0)
 
 
 def accept_longest_path(cu_nodes, parent, draft_tok, target_argmax, accept_len=None,

@@ -40,6 +40,7 @@
 #include <atomic>
 #include <cstdio>
 
+#include "tc_pipeline.cuh"
 #include "tc_ptx.cuh"
 #include "tva_internal.h"
 
@@ -51,9 +52,7 @@ using namespace ptx;
 constexpr int kThreadsTc = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr uint64_t kDrainNs = 2000000000ull;  // drain waits, and the default main-loop limit
 constexpr int kHalfBytes = 128 * 128;  // 128 rows of 64 bf16 (one 128-byte swizzle span)
-constexpr uint32_t kNegInfBits = 0xff800000u;
 
 template <int D>
 struct Cfg {
@@ -80,40 +79,12 @@ struct TcArgs {
 std::atomic<unsigned long long> g_wait_limit_ns{0};
 std::atomic<int> g_force_stall{0};
 
-struct Segment {
-  Loc L;
-  int tile0, n;
-};
-
-__device__ __forceinline__ bool next_segment(const Problem& pr, long long& t, long long t_end,
-                                             Segment& s) {
-  if (t >= t_end) return false;
-  s.L = locate_unit(pr, t);
-  const long long seg_end = min(t_end, s.L.start + s.L.tiles);
-  s.tile0 = s.L.tile;
-  s.n = (int)(seg_end - t);
-  t = seg_end;
-  return true;
-}
-
 // Q buffers: with one M-tile per row group (W = 1) the Q region holds two M-tiles, so
 // segments alternate between two buffers and the next segment's Q is loaded while the
 // current one is still in use; with W = 2 one buffer holds both M-tiles.
 __device__ __forceinline__ int q_buffer(int W, int sg) { return W == 1 ? (sg & 1) : 0; }
 // Earlier segments that used the same buffer.
 __device__ __forceinline__ int q_use(int W, int sg) { return W == 1 ? (sg >> 1) : sg; }
-
-// A bounded wait taken by a whole converged warp; the result is the same in every lane.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, limit_ns));
-}
-
-// Waits that ignore the abort flag (used only while draining).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
-  volatile int never = 0;
-  mbar_wait(bar, parity, &never, kDrainNs);
-}
 
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(kThreadsTc, 1)
@@ -671,6 +642,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // 3-D 16-bit map over [rows][heads][d] with a box of {64, box_heads, box_rows}.
 bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int d, int heads, long long rows,
               int box_heads, int box_rows) {
@@ -693,6 +666,14 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int d,
   return true;
 }
 
+void tc_wait_settings(uint64_t* wait_ns, int* stall) {
+  const unsigned long long lim = g_wait_limit_ns.load(std::memory_order_relaxed);
+  *wait_ns = lim > 0 ? (uint64_t)lim : kDrainNs;
+  *stall = g_force_stall.load(std::memory_order_relaxed);
+}
+
+namespace {
+
 template <int D, bool kBF16>
 cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s) {
   constexpr CUtensorMapDataType type = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -711,8 +692,8 @@ cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                              "cudaFuncSetAttribute(partials_tc_kernel)");
   if (e != cudaSuccess) return e;
-  const unsigned long long lim = g_wait_limit_ns.load(std::memory_order_relaxed);
-  TcArgs ta{a, W, npt, lim > 0 ? (uint64_t)lim : kDrainNs, g_force_stall.load(std::memory_order_relaxed)};
+  TcArgs ta{a, W, npt, 0, 0};
+  tc_wait_settings(&ta.wait_ns, &ta.stall);
   e = launch_pdl(partials_tc_kernel<D, kBF16>, dim3(pr.U), dim3(kThreadsTc), (size_t)smem, s, mq, mk, mv, mtk,
                  mtv, ta);
   if (e != cudaSuccess) {

@@ -30,6 +30,9 @@ using tva::Problem;
 
 constexpr int kMaxDevices = 64;
 
+// tva_diag_use_cta_pair: non-zero selects the CTA-pair partials kernel where it applies.
+std::atomic<int> g_use_cta_pair{0};
+
 int device_sms(int* sms) {
   int dev = 0;
   if (tva::check_cuda(cudaGetDevice(&dev), "cudaGetDevice") != cudaSuccess || dev < 0 ||
@@ -69,6 +72,7 @@ tva_status check_shape(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
 struct Layout {
   Problem pr;
   int W, npt;
+  bool pair;  // row groups of two M-tiles at head_dim 128 (16-bit): the CTA-pair kernel
   size_t o_bytes, lse_bytes, total;
   long long slots;
 };
@@ -99,7 +103,11 @@ tva_status make_layout(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
   pr.single_nodes = single_nodes;
   pr.B = B; pr.Hq = Hq; pr.Hkv = Hkv; pr.G = G; pr.d = d;
   pr.RG = W * npt * G;
-  pr.U = dtype == TVA_FP32 ? sms * tva::simt_workers_per_sm() : sms;  // the tensor-core kernels: one CTA per SM
+  // workers: the fp32 kernel runs several CTAs per SM; the tensor-core kernel one CTA per
+  // SM, the CTA-pair kernel (selected by tva_diag_use_cta_pair; two M-tiles per row group,
+  // head_dim 128) one pair per two SMs
+  L->pair = g_use_cta_pair.load(std::memory_order_relaxed) != 0 && dtype != TVA_FP32 && W == 2 && d == 128;
+  pr.U = dtype == TVA_FP32 ? sms * tva::simt_workers_per_sm() : (L->pair ? sms / 2 : sms);
   pr.max_prefix = max_prefix; pr.max_nodes = max_nodes;
   pr.kv_capacity = kv_cap; pr.node_capacity = node_cap;
   const long long groups = (long long)B * Hkv * ((max_nodes + W * npt - 1) / (W * npt));
@@ -137,7 +145,8 @@ tva_status run_partials(const Layout& L, int dtype, float softmax_scale, const v
   a.slots = L.slots;
   a.status = dev_status;
   const cudaError_t e = dtype == TVA_FP32 ? tva::launch_partials_simt(a, dtype, s)
-                                          : tva::launch_partials_tc(a, dtype == TVA_BF16, L.W, L.npt, s);
+                        : L.pair           ? tva::launch_partials_pair(a, dtype == TVA_BF16, L.npt, s)
+                                           : tva::launch_partials_tc(a, dtype == TVA_BF16, L.W, L.npt, s);
   return e == cudaSuccess ? TVA_OK : TVA_ERR_CUDA;
 }
 
@@ -344,6 +353,8 @@ tva_status tva_read_device_status(int32_t* host_status, void* stream) {
 void tva_diag_set_wait_limit(unsigned long long wait_limit_ns, int force_stall) {
   tva::set_tc_wait_limit(wait_limit_ns, force_stall);
 }
+
+void tva_diag_use_cta_pair(int enable) { g_use_cta_pair.store(enable != 0 ? 1 : 0, std::memory_order_relaxed); }
 
 void tva_release(void) {
   std::lock_guard<std::mutex> lock(g_owned_mu);

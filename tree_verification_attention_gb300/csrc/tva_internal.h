@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <utility>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "tva_common.cuh"
@@ -123,6 +124,14 @@ int simt_workers_per_sm();
 cudaError_t launch_partials_simt(const PartialArgs& a, int dtype, cudaStream_t s);
 // bf16 (bf16 = true) or fp16, head_dim 64 or 128; W M-tiles of npt nodes per row group
 cudaError_t launch_partials_tc(const PartialArgs& a, bool bf16, int W, int npt, cudaStream_t s);
+// Row groups of two M-tiles at head_dim 128 on CTA pairs (a.pr.U = pairs); bf16 or fp16.
+cudaError_t launch_partials_pair(const PartialArgs& a, bool bf16, int npt, cudaStream_t s);
+// 3-D 16-bit tensor map over [rows][heads][d] with a box of {64, box_heads, box_rows}
+// (128-byte swizzle); false (and tva_last_error) if the driver rejects it.
+bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int d, int heads, long long rows,
+              int box_heads, int box_rows);
+// Main-loop wait limit and test stall for the tensor-core partials kernels.
+void tc_wait_settings(uint64_t* wait_ns, int* stall);
 // Main-loop wait limit of the tensor-core partials kernel for later launches (0: the
 // default 2 s) and the test stall (tva_diag_set_wait_limit).
 void set_tc_wait_limit(unsigned long long ns, int stall);
