@@ -54,6 +54,11 @@ EDGE = [
     # segments alternate between the two Q buffers of one-M-tile row groups
     dict(batch=40, Hq=32, Hkv=8, d=128, prefix=(50, 300), m=8, tree="random", dtype="bf16", vocab=8),
     dict(batch=24, Hq=16, Hkv=4, d=64, prefix=(0, 260), m=12, tree="random", dtype="fp16", vocab=8),
+    # trees a few nodes past two M-tiles: the last row group of each sequence computes one
+    # M-tile (weight 1) and the others two, so workers' ranges mix both kinds of segment
+    dict(batch=5, Hq=32, Hkv=8, d=128, prefix=(100, 2000), m=70, tree="random", dtype="bf16", vocab=8),
+    dict(batch=2, Hq=12, Hkv=4, d=128, prefix=(300, 900), m=100, tree="random", dtype="bf16", vocab=8),
+    dict(batch=4, Hq=32, Hkv=8, d=128, prefix=(0, 600), m=68, tree="random", dtype="fp16", vocab=8),
     # float16 (LongSpec's precision): d = 64 and 128, a ragged batch, a full 128-node tree
     dict(batch=3, Hq=8, Hkv=2, d=64, prefix=(0, 400), m=21, tree="random", dtype="fp16", vocab=8),
     dict(batch=1, Hq=32, Hkv=8, d=128, prefix=300, m=128, tree="random", dtype="fp16", vocab=8),
