@@ -25,29 +25,29 @@
 //             CTA announces its own bytes.
 //   warp 9    MMA issue, first CTA only (converged warp, one elected lane); in the other
 //             CTA it only takes part in the TMEM allocation.
-//   warps 0-7 softmax of the CTA's 128 rows: warps 0-3 take keys 0-63 of each tile and
-//             warps 4-7 keys 64-127 (warps w and w + 4 share TMEM lanes, i.e. rows); the
-//             two halves exchange row maxima through shared memory once a tile and row
-//             sums once a segment.
-// TMEM per CTA: S buffers at columns 0 and 128 (tiles alternate), O at 256, P buffers at
-// 384 and 448.  With two S buffers the softmax of tile j + 1 never waits for the PV of
-// tile j: the MMA order is S(0), S(1), PV(0), S(2), PV(1), S(3), ...  The running max
-// moves only when it grows by more than 2^8; when it does, O is rescaled in TMEM once the
-// previous tile's PV has completed (a commit after every PV says when).
+//   warps 0-7 softmax: two streams of 4 warps; stream w takes the segment's tiles j with
+//             j & 1 == w, and thread r of a stream owns TMEM lane (= row of this CTA's
+//             M-tile) r and all 128 keys of a tile.  The two streams' partials are merged
+//             in the epilogue.
+// TMEM per CTA: stream w's S buffer at columns 128 w (P overwrites its first 64 columns
+// as packed 16-bit pairs) and its O accumulator at 256 + 128 w.  The MMA order is
+//   S_0(0), S_1(1), PV_0(0), S_0(2), PV_1(1), S_1(3), ...
+// so each stream's softmax overlaps the other stream's MMAs, and the commit that
+// publishes S_w(j + 2) also covers PV_w(j): a stream may rescale its O (when its running
+// max grows by more than 2^8) as soon as its S is ready.  Each CTA collects its threads'
+// release of O on a local barrier; one thread per CTA passes it to the first CTA.
 //
-// Every wait is bounded (mbarriers and %globaltimer; the two softmax halves synchronise
-// through mbarriers, never through an unbounded named barrier); a CTA whose wait expires
-// raises its own and its peer's abort flag, records TVA_ERR_TIMEOUT, drains and frees
-// TMEM.  Both CTAs meet at a cluster barrier before the TMEM is released, so neither
-// leaves while the other's MMAs or arrivals may still touch it.
+// Every wait is bounded (mbarriers and %globaltimer); a CTA whose wait expires raises its
+// own and its peer's abort flag, records TVA_ERR_TIMEOUT, drains and frees TMEM.  Both
+// CTAs meet at a cluster barrier before the TMEM is released, so neither leaves while
+// the other's MMAs or arrivals may still touch it.
 //
-// Status: selected only through tva_diag_use_cta_pair.  Measured per launch it is slower
-// than the one-SM kernel on every workload it applies to (64k prefix, 64-node tree:
-// 55.6 vs 52.2 us; 128k prefix, 128-node tree, G = 8: 412 vs 382 us; the 68-node beam
-// tree: even).  Per-tile timestamps show why: each CTA has one softmax stream, so the
-// tensor pipe's PV(j) + S(j + 2) and the softmax of tile j + 1 form one chain (about
-// 0.95 us a tile), where the one-SM kernel's two streams each overlap the other's MMAs;
-// the halved operand traffic does not pay for that.
+// Status: selected only through tva_diag_use_cta_pair.  Measured per launch it does not
+// beat the one-SM kernel on the workloads it applies to (64k prefix, 64-node tree: 55.8
+// vs 51.8 us; 128k prefix, 128-node tree, G = 8, tensor-bound: 381 vs 378 us; the
+// 68-node beam tree: even).  Halving the shared-memory operand reads per SM did not
+// lift the tensor-bound case, so those reads are not what limits the one-SM kernel
+// there.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -74,8 +74,8 @@ constexpr int kBarOff = 2 * kQBuf + kStages * kStageBytes;   // 192 KB
 // misc region (offsets from kBarOff)
 constexpr int kMiscTmem = 256;               // TMEM base address, then the abort flag
 constexpr int kCnt = 272;                    // int [4]: K/V copies per CTA, Q copies per CTA
-constexpr int kMx = 512;                     // float [2][2][128] row maxima (tile parity, half, row)
-constexpr int kLs = 2560;                    // float [2][2][128] row sums (segment parity, half, row)
+constexpr int kM1 = 512;                     // float [2][128] stream 1's row maxima (segment parity, row)
+constexpr int kL1 = 1536;                    // float [2][128] stream 1's row sums
 constexpr int kPar = 4608;                   // int [128] parent ids of the tree tile
 constexpr int kPr = 5120;                    // Problem (staged)
 constexpr int kCuOff = 5376;                 // staged cu_* arrays
@@ -113,19 +113,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t KV_EMPTY = bar0 + 64;                  // [kStages]
   const uint32_t Q_FULL = bar0 + 128;                   // [2], used in the first CTA
   const uint32_t Q_EMPTY = bar0 + 144;                  // [2]
-  const uint32_t S_FULL = bar0 + 160;                   // [2]
-  const uint32_t P_FULL = bar0 + 176;                   // [2], used in the first CTA
-  const uint32_t PV_DONE = bar0 + 192;
-  const uint32_t O_FULL = bar0 + 200;
+  const uint32_t S_FULL = bar0 + 160;                   // [2] by stream
+  const uint32_t P_FULL = bar0 + 176;                   // [2] by stream, used in the first CTA
+  const uint32_t O_FULL = bar0 + 192;                   // [2] by stream
   const uint32_t O_FREE = bar0 + 208;                   // used in the first CTA
   const uint32_t DRAIN = bar0 + 216;                    // used in the first CTA
-  const uint32_t XCH = bar0 + 224;                      // [2] row-maxima exchange (by tile parity)
-  const uint32_t LX = bar0 + 240;                       // row-sum exchange
-  const uint32_t PAR = bar0 + 248;                      // parent ids staged
+  const uint32_t SEG_DONE = bar0 + 224;                 // this CTA's softmax threads are done with O
+  const uint32_t M1_READY = bar0 + 232;                 // stream 1's row max / sum published
+  const uint32_t PAR = bar0 + 240;                      // parent ids staged
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kBarOff + kMiscTmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kBarOff + kMiscTmem + 4);
-  float* mx_s = reinterpret_cast<float*>(smem + kBarOff + kMx);
-  float* ls_s = reinterpret_cast<float*>(smem + kBarOff + kLs);
+  float* m1_s = reinterpret_cast<float*>(smem + kBarOff + kM1);
+  float* l1_s = reinterpret_cast<float*>(smem + kBarOff + kL1);
   int* par_s = reinterpret_cast<int*>(smem + kBarOff + kPar);
   // the first CTA's copies of the barriers it collects arrivals on, and the peer's abort flag
   const uint32_t kv_full0 = mapa_shared(KV_FULL, 0), q_full0 = mapa_shared(Q_FULL, 0);
@@ -147,15 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(Q_FULL + 8 * b, 2);
       mbar_init(Q_EMPTY + 8 * b, 1);
       mbar_init(S_FULL + 8 * b, 1);
-      mbar_init(P_FULL + 8 * b, 16);    // 8 softmax warps in each CTA
-      mbar_init(XCH + 8 * b, 256);
+      mbar_init(P_FULL + 8 * b, 8);     // the stream's 4 warps in each CTA
+      mbar_init(O_FULL + 8 * b, 1);
     }
-    mbar_init(PV_DONE, 1);
-    mbar_init(O_FULL, 1);
-    mbar_init(O_FREE, 16);
+    mbar_init(O_FREE, 2);               // one arrival from each CTA
     mbar_init(DRAIN, 1);
-    mbar_init(LX, 256);
-    mbar_init(PAR, 256);
+    mbar_init(SEG_DONE, 256);
+    mbar_init(M1_READY, 128);
+    mbar_init(PAR, 128);
     *abort_flag = 0;
     fence_mbar_init();
     __threadfence_block();
@@ -259,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (rank == 0) {
       constexpr uint32_t idesc_s = idesc_bf16(256, 128, false, kBF16);
       constexpr uint32_t idesc_o = idesc_bf16(256, 128, true, kBF16);
-      int ring = 0, sg = 0, tg = 0;  // ring position, segment, tiles before this segment
+      int ring = 0, sg = 0;
+      uint32_t pbits = 0;  // bit w: parity of the next P_FULL[w] phase
       bool ok = true;
       long long t = t_begin;
       Segment S;
@@ -276,27 +275,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t k_lo = (uint32_t)sdesc_sw128(kv_s, 16, 1024);
       const uint32_t v_lo = (uint32_t)sdesc_sw128(kv_s, kStageBytes, 1024);
       const uint32_t q_lo = (uint32_t)sdesc_sw128(q_s, 16, 1024);
-      auto issue_s = [&](int tile_g, int qb, int idx) {
+      // S of stream w into its buffer (TMEM columns 128 w)
+      auto issue_s = [&](int w, int qb, int idx) {
         const uint32_t kl = k_lo + (uint32_t)((idx % kStages) * kStageBytes >> 4);
         const uint32_t ql = q_lo + (uint32_t)(qb * kQBuf >> 4);
-        const uint32_t dt = tmem + 128 * (tile_g & 1);
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
           const uint32_t oq = (uint32_t)((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
           const uint32_t ok_ = (uint32_t)((ks >> 2) * (kStageBytes / 2) + (ks & 3) * 32) >> 4;
-          mma2_ss_elect(dt, desc_join(ql + oq, k_hi), desc_join(kl + ok_, k_hi), idesc_s, ks > 0);
+          mma2_ss_elect(tmem + 128 * w, desc_join(ql + oq, k_hi), desc_join(kl + ok_, k_hi), idesc_s, ks > 0);
         }
-        tc_commit2_elect(S_FULL + 8 * (tile_g & 1), 3);
+        tc_commit2_elect(S_FULL + 8 * w, 3);
         tc_commit2_elect(KV_EMPTY + 8 * (idx % kStages), 3);
       };
-      auto issue_pv = [&](int tile_g, int idx, bool acc) {
+      // O_w += P_w V, P_w read from the first 64 columns of stream w's S buffer
+      auto issue_pv = [&](int w, int idx, bool acc) {
         const uint32_t vl = v_lo + (uint32_t)((idx % kStages) * kStageBytes >> 4);
-        const uint32_t at = tmem + 384 + 64 * (tile_g & 1);
 #pragma unroll
         for (int ks = 0; ks < kKeyTile / 16; ++ks)
-          mma2_ts_elect(tmem + 256, at + ks * 8, desc_join(vl + (uint32_t)(ks * 2048 >> 4), v_hi), idesc_o,
-                        (acc || ks > 0) ? 1u : 0u);
-        tc_commit2_elect(PV_DONE, 3);
+          mma2_ts_elect(tmem + 256 + 128 * w, tmem + 128 * w + ks * 8,
+                        desc_join(vl + (uint32_t)(ks * 2048 >> 4), v_hi), idesc_o, (acc || ks > 0) ? 1u : 0u);
         tc_commit2_elect(KV_EMPTY + 8 * (idx % kStages), 3);
       };
       // Test hook: DRAIN's first phase completes only through this thread's own commit
@@ -304,37 +302,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (args.stall && !wait_or_abort(warp_wait(DRAIN, 0, abort_flag, wait_ns))) ok = false;
       while (ok && next_segment(pr, t, t_end, S)) {
         const int n = S.n, qb = sg & 1;
-        // ring order: K0, K1, then V_j followed by K_{j+2}
+        // ring order: K0, K1, then V_j followed by K_{j+2}; tile j belongs to stream j & 1
         auto rK = [&](int k) { return ring + (k < 2 ? k : 2 * k - 1); };
         auto rV = [&](int j) { return ring + (j <= n - 2 ? 2 + 2 * j : 2 * n - 1); };
         if (!(ok = wait_or_abort(warp_wait(Q_FULL + 8 * qb, (sg >> 1) & 1, abort_flag, wait_ns)))) break;
         tc_fence_after();
         if (!(ok = wait_kv(rK(0)))) break;
-        issue_s(tg, qb, rK(0));
+        issue_s(0, qb, rK(0));
         if (n > 1) {
           if (!(ok = wait_kv(rK(1)))) break;
-          issue_s(tg + 1, qb, rK(1));
+          issue_s(1, qb, rK(1));
         }
         if (n <= 2) tc_commit2_elect(Q_EMPTY + 8 * qb, 3);
         for (int j = 0; j < n && ok; ++j) {
-          const int tj = tg + j;
-          if (!(ok = wait_or_abort(warp_wait(P_FULL + 8 * (tj & 1), (tj >> 1) & 1, abort_flag, wait_ns)))) break;
+          const int w = j & 1;
+          if (!(ok = wait_kv(rV(j)))) break;
+          if (!(ok = wait_or_abort(warp_wait(P_FULL + 8 * w, (pbits >> w) & 1u, abort_flag, wait_ns)))) break;
           tc_fence_after();
-          if (j == 0 && sg > 0) {  // the previous segment's O has been read by both CTAs
+          pbits ^= 1u << w;
+          if (j == 0 && sg > 0) {  // both CTAs have read the previous segment's O
             if (!(ok = wait_or_abort(warp_wait(O_FREE, (sg - 1) & 1, abort_flag, wait_ns)))) break;
             tc_fence_after();
           }
-          if (!(ok = wait_kv(rV(j)))) break;
-          issue_pv(tj, rV(j), j > 0);
-          if (j == n - 1) tc_commit2_elect(O_FULL, 3);
+          issue_pv(w, rV(j), j >= 2);
+          if (j + 2 >= n) tc_commit2_elect(O_FULL + 8 * w, 3);
           if (j + 2 < n) {
             if (!(ok = wait_kv(rK(j + 2)))) break;
-            issue_s(tj + 2, qb, rK(j + 2));
+            issue_s(w, qb, rK(j + 2));
             if (j + 2 == n - 1) tc_commit2_elect(Q_EMPTY + 8 * qb, 3);
           }
         }
         ring += 2 * n;
-        tg += n;
         ++sg;
       }
       // drain: every MMA issued here (on either CTA's memory) has completed
@@ -343,11 +341,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ softmax
-    const int wg = warp >> 2;                 // 0: keys 0-63 of a tile, 1: keys 64-127
-    const int r = threadIdx.x & 127;          // TMEM lane = row of this CTA's M-tile
+    // Two streams of 4 warps; stream w takes the segment's tiles j with j & 1 == w, thread
+    // r of a stream owns TMEM lane (= row of this CTA's M-tile) r and all 128 keys of a
+    // tile.  A stream's running max moves only when it grows by more than 2^8 (stale
+    // maxima cancel in the final division); then its O is rescaled in TMEM, which is
+    // safe once its S is ready: the commit that publishes S_w(j + 2) follows PV_w(j).
+    const int w = warp >> 2;
+    const int r = threadIdx.x & 127;
     const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = 128 * w, o_col = 256 + 128 * w;
     const float sl2 = a.scale_log2;
-    int tg = 0, sg = 0, trees = 0;
+    // phase parities: bit 0 this stream's S_FULL, 1 / 2 O_FULL[0] / O_FULL[1], 3 PAR
+    uint32_t ph = 0;
+    int sg = 0;
     bool ok = true;
     long long t = t_begin;
     Segment S;
@@ -360,136 +366,177 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int node = (L.mp * 2 + (int)rank) * npt + r / G;  // local node id of this row
       bool row_ok = r < npt * G && node < L.s.m;
       uint32_t anc[4] = {0u, 0u, 0u, 0u};
-      if (S.tile0 == 0) {  // the tree tile: the row's ancestor bits, found while K0 loads
-        if (wg == 0 && r < L.s.m) par_s[r] = __ldg(a.parent + L.s.n0 + r);
+      if (S.tile0 == 0 && w == 0) {  // the tree tile (stream 0's): ancestor bits while K0 loads
+        if (r < L.s.m) par_s[r] = __ldg(a.parent + L.s.n0 + r);
         mbar_arrive(PAR);
-        if (!(ok = bwait(PAR, trees & 1))) break;
-        ++trees;
+        if (!(ok = bwait(PAR, (ph >> 3) & 1))) break;
+        ph ^= 8u;
         if (row_ok && !ancestor_bits_shared(par_s, node, anc)) set_status(a.status, kStatusBadTree);
       }
+      const int n_mine = (n - w + 1) / 2;
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < n; ++j, ++tg) {
-        const int b = tg & 1;
-        if (!(ok = bwait(S_FULL + 8 * b, (tg >> 1) & 1))) break;
-        tc_fence_after();
-        const int tile = S.tile0 + j;
+      for (int i = 0; i < n_mine; ++i) {
+        const int tile = S.tile0 + 2 * i + w;
         const bool is_tree = tile == 0;
-        const uint32_t s_col = 128 * b + 64 * wg;
+        if (!(ok = bwait(S_FULL + 8 * w, ph & 1))) break;
+        tc_fence_after();
         // keys of this tile: [0, lim) exist; the tree tile also needs the ancestor bit
         const int lim = is_tree ? L.s.m : min(kKeyTile, L.s.P - (tile - 1) * kKeyTile);
-        uint32_t s[64];
-        tmem_ld32(tl + s_col, s);
-        tmem_ld32(tl + s_col + 32, s + 32);
-        tmem_wait_ld32(s);
-        tie32(s + 32);
         if (is_tree || lim < kKeyTile) {  // rare tiles: logits the row does not see -> -inf
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int key0 = 64 * wg + 32 * c;
-            const int rem = lim - key0;
+#pragma unroll 1
+          for (int ck = 0; ck < 4; ++ck) {
+            uint32_t sv[32];
+            tmem_ld32(tl + s_col + 32 * ck, sv);
+            tmem_wait_ld32(sv);
+            const int rem = lim - 32 * ck;
             uint32_t vw = rem >= 32 ? 0xffffffffu : (rem <= 0 ? 0u : (1u << rem) - 1u);
-            if (is_tree) vw &= row_ok ? anc[key0 >> 5] : 0u;
+            if (is_tree) {
+              const uint32_t aw = ck == 0 ? anc[0] : ck == 1 ? anc[1] : ck == 2 ? anc[2] : anc[3];
+              vw &= row_ok ? aw : 0u;
+            }
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (!((vw >> e) & 1u)) s[32 * c + e] = kNegInfBits;
+              if (!((vw >> e) & 1u)) sv[e] = kNegInfBits;
+            tmem_st32(tl + s_col + 32 * ck, sv);
           }
+          tmem_wait_st();
         }
+        // pass 1: row maximum, 64 TMEM columns at a time
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
-          mx0 = max3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-          mx1 = max3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[64];
+          tmem_ld32(tl + s_col + 64 * h, sv);
+          tmem_ld32(tl + s_col + 64 * h + 32, sv + 32);
+          tmem_wait_ld32(sv);
+          tie32(sv + 32);
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            mx0 = max3(mx0, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+            mx1 = max3(mx1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+          }
         }
-        const float m_half = fmaxf(mx0, mx1) * sl2;
-        // exchange with the other half of the row
-        float* mx_t = mx_s + (tg & 1) * 256;
-        mx_t[wg * 128 + r] = m_half;
-        mbar_arrive(XCH + 8 * b);
-        if (!(ok = bwait(XCH + 8 * b, (tg >> 1) & 1))) break;
-        const float m_new = fmaxf(m_run, fmaxf(m_half, mx_t[(wg ^ 1) * 128 + r]));
-        if (j == 0) {
+        const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
+        if (i == 0) {
           m_run = m_new;
         } else {
           const bool need = m_new > m_run + 8.0f;
           if (__any_sync(0xffffffffu, need)) {
-            // O is still being accumulated by the previous tile's PV: wait for it, then
-            // rescale this half's columns of O (both halves take the same decision)
-            if (!(ok = bwait(PV_DONE, (tg - 1) & 1))) break;
-            tc_fence_after();
             const float alpha = need ? ex2(m_run - m_new) : 1.f;
             if (need) {
               l_run *= alpha;
               m_run = m_new;
             }
 #pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 32) {
+            for (int c0 = 0; c0 < kD; c0 += 32) {
               uint32_t o[32];
-              tmem_ld32(tl + 256 + 64 * wg + c0, o);
+              tmem_ld32(tl + o_col + c0, o);
               tmem_wait_ld32(o);
 #pragma unroll
               for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st32(tl + 256 + 64 * wg + c0, o);
+              tmem_st32(tl + o_col + c0, o);
             }
             tmem_wait_st();
           }
         }
         const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
-        // p = 2^(s * scale - m), packed into this half's columns of P buffer b
+        // pass 2: p = 2^(s * scale - m), packed as 16-bit pairs into the already-read
+        // first half of the S buffer (P columns 32 h.. come from S columns 64 h..)
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nbx2 = f2_pack(nb, nb);
         uint64_t lsx2 = f2_pack(0.f, 0.f);
-        uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2x2, nbx2), x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          lsx2 = f2_add(lsx2, f2_pack(p0, p1));
-          pk[c] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sv[64];
+          tmem_ld32(tl + s_col + 64 * h, sv);
+          tmem_ld32(tl + s_col + 64 * h + 32, sv + 32);
+          tmem_wait_ld32(sv);
+          tie32(sv + 32);
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), sl2x2, nbx2),
+                      x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            lsx2 = f2_add(lsx2, f2_pack(p0, p1));
+            pk[c] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+          }
+          tmem_st32(tl + s_col + 32 * h, pk);
         }
-        tmem_st32(tl + 384 + 64 * b + 32 * wg, pk);
         float ls0, ls1;
         f2_unpack(lsx2, ls0, ls1);
         l_run += ls0 + ls1;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(p_full0 + 8 * b);
+        if (lane == 0) mbar_arrive_cluster(p_full0 + 8 * w);
+        ph ^= 1u;
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
-      if (!(ok = bwait(O_FULL, sg & 1))) break;
-      tc_fence_after();
-      float* ls_t = ls_s + (sg & 1) * 256;
-      ls_t[wg * 128 + r] = l_run;
-      mbar_arrive(LX);
-      if (!(ok = bwait(LX, sg & 1))) break;
-      const float l_tot = l_run + ls_t[(wg ^ 1) * 128 + r];
-      const size_t slot = (size_t)u + L.q;
-      if (slot >= (size_t)a.slots) {  // cannot happen for a consistent layout; never write past it
-        set_status(a.status, kStatusInvalidArg);
-        row_ok = false;
-      }
-      const int pp = (int)rank * 128 + r;  // padded row: lane = row within a 32-row block
-      if (row_ok && !TVA_CHECK(node >= 0 && node < L.s.m, a.status)) row_ok = false;
-      float* oblk = a.o_part + o_part_offset(slot, pp, 0, 256, kD);
-      const float inv = 1.f / l_tot;
+      // Stream 1 hands its row max / sum to stream 0, which merges the two O accumulators.
+      // Each CTA's release of O is collected on SEG_DONE and passed to the first CTA's
+      // O_FREE by one thread, so neither stream can arrive for the next segment before
+      // this segment's phase is complete.
+      if (w == 1) {
+        if (sg > 0 && !(ok = bwait(SEG_DONE, (sg - 1) & 1))) break;
+        m1_s[(sg & 1) * 128 + r] = m_run;
+        l1_s[(sg & 1) * 128 + r] = l_run;
+        mbar_arrive(M1_READY);
+        mbar_arrive(SEG_DONE);
+      } else {
+        if (!(ok = bwait(M1_READY, sg & 1))) break;
+        const float m1 = m1_s[(sg & 1) * 128 + r];
+        const float l1 = l1_s[(sg & 1) * 128 + r];
+        const bool has1 = n > 1;
+        if (!(ok = bwait(O_FULL, (ph >> 1) & 1))) break;
+        ph ^= 2u;
+        if (has1) {
+          if (!(ok = bwait(O_FULL + 8, (ph >> 2) & 1))) break;
+          ph ^= 4u;
+        }
+        tc_fence_after();
+        const float mm = has1 ? fmaxf(m_run, m1) : m_run;
+        const float a0 = (m_run == -INFINITY) ? 0.f : ex2(m_run - mm);
+        const float a1 = (!has1 || m1 == -INFINITY) ? 0.f : ex2(m1 - mm);
+        const float lt = a0 * l_run + a1 * l1;
+        const float inv = 1.f / lt;
+        const float w0 = a0 * inv, w1 = a1 * inv;
+        const size_t slot = (size_t)u + L.q;
+        if (slot >= (size_t)a.slots) {  // cannot happen for a consistent layout; never write past it
+          set_status(a.status, kStatusInvalidArg);
+          row_ok = false;
+        }
+        const int pp = (int)rank * 128 + r;  // padded row: lane = row within a 32-row block
+        if (row_ok && !TVA_CHECK(node >= 0 && node < L.s.m, a.status)) row_ok = false;
+        float* oblk = a.o_part + o_part_offset(slot, pp, 0, 256, kD);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(tl + 256 + 64 * wg + c0, o);
-        tmem_wait_ld32(o);
-        if (row_ok) {
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t o[32], o1[32];
+          tmem_ld32(tl + 256 + c0, o);
+          tmem_ld32(tl + 384 + c0, o1);
+          tmem_wait_ld32(o);
+          tie32(o1);
+          if (row_ok) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(oblk + (64 * wg + c0 + e) * 32) =
-                make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                            __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            for (int e = 0; e < 32; e += 4) {
+              float4 v;
+              v.x = __uint_as_float(o[e]) * w0 + (has1 ? __uint_as_float(o1[e]) * w1 : 0.f);
+              v.y = __uint_as_float(o[e + 1]) * w0 + (has1 ? __uint_as_float(o1[e + 1]) * w1 : 0.f);
+              v.z = __uint_as_float(o[e + 2]) * w0 + (has1 ? __uint_as_float(o1[e + 2]) * w1 : 0.f);
+              v.w = __uint_as_float(o[e + 3]) * w0 + (has1 ? __uint_as_float(o1[e + 3]) * w1 : 0.f);
+              *reinterpret_cast<float4*>(oblk + (c0 + e) * 32) = v;
+            }
+          }
+        }
+        if (row_ok) a.lse_part[slot * 256 + pp] = mm + log2f(lt);
+        tc_fence_before();
+        mbar_arrive(SEG_DONE);
+        if (warp == 0) {
+          if (!(ok = bwait(SEG_DONE, sg & 1))) break;
+          if (lane == 0) mbar_arrive_cluster(o_free0);
         }
       }
-      if (row_ok && wg == 0) a.lse_part[slot * 256 + pp] = m_run + log2f(l_tot);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(o_free0);
       ++sg;
     }
   }
