@@ -401,17 +401,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_wait_st();
         }
-        // pass 1: row maximum, 64 TMEM columns at a time
+        // pass 1: row maximum; all 128 columns loaded before the one wait (each
+        // tcgen05.wait::ld is a full TMEM round trip on the critical path)
         float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sv[64];
-          tmem_ld32(tl + s_col + 64 * h, sv);
-          tmem_ld32(tl + s_col + 64 * h + 32, sv + 32);
+        {
+          uint32_t sv[128];
+          tmem_ld32(tl + s_col, sv);
+          tmem_ld32(tl + s_col + 32, sv + 32);
+          tmem_ld32(tl + s_col + 64, sv + 64);
+          tmem_ld32(tl + s_col + 96, sv + 96);
           tmem_wait_ld32(sv);
           tie32(sv + 32);
+          tie32(sv + 64);
+          tie32(sv + 96);
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
+          for (int c = 0; c < 128; c += 4) {
             mx0 = max3(mx0, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
             mx1 = max3(mx1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
           }
@@ -444,24 +448,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first half of the S buffer (P columns 32 h.. come from S columns 64 h..)
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nbx2 = f2_pack(nb, nb);
         uint64_t lsx2 = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sv[64];
-          tmem_ld32(tl + s_col + 64 * h, sv);
-          tmem_ld32(tl + s_col + 64 * h + 32, sv + 32);
+        {
+          uint32_t sv[128];
+          tmem_ld32(tl + s_col, sv);
+          tmem_ld32(tl + s_col + 32, sv + 32);
+          tmem_ld32(tl + s_col + 64, sv + 64);
+          tmem_ld32(tl + s_col + 96, sv + 96);
           tmem_wait_ld32(sv);
           tie32(sv + 32);
-          uint32_t pk[32];
+          tie32(sv + 64);
+          tie32(sv + 96);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1])), sl2x2, nbx2),
-                      x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            lsx2 = f2_add(lsx2, f2_pack(p0, p1));
-            pk[c] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+          for (int h = 0; h < 2; ++h) {
+            // the packed pairs of keys 64 h .. 64 h + 63 overwrite sv[32 h ..], already read
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[64 * h + 2 * c]), __uint_as_float(sv[64 * h + 2 * c + 1])),
+                               sl2x2, nbx2),
+                        x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              lsx2 = f2_add(lsx2, f2_pack(p0, p1));
+              sv[32 * h + c] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            }
           }
-          tmem_st32(tl + s_col + 32 * h, pk);
+          tmem_st32(tl + s_col, sv);
+          tmem_st32(tl + s_col + 32, sv + 32);
         }
         float ls0, ls1;
         f2_unpack(lsx2, ls0, ls1);

@@ -453,17 +453,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
           }
           tmem_wait_st();
         }
-        // pass 1: row maximum, 64 TMEM columns at a time
+        // pass 1: row maximum.  All 128 columns are loaded before the one wait:
+        // tcgen05.wait::ld waits for every load of the thread, so each wait is a full TMEM
+        // round trip on the softmax's critical path (two per pass cost 1.5-2 us a launch).
         float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t s[64];
-          tmem_ld32(tl + s_col + 64 * h, s);
-          tmem_ld32(tl + s_col + 64 * h + 32, s + 32);
+        {
+          uint32_t s[128];
+          tmem_ld32(tl + s_col, s);
+          tmem_ld32(tl + s_col + 32, s + 32);
+          tmem_ld32(tl + s_col + 64, s + 64);
+          tmem_ld32(tl + s_col + 96, s + 96);
           tmem_wait_ld32(s);
           tie32(s + 32);
+          tie32(s + 64);
+          tie32(s + 96);
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
+          for (int c = 0; c < 128; c += 4) {
             mx0 = max3(mx0, __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
             mx1 = max3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
           }
@@ -493,28 +498,36 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         }
         const float nb = (m_run == -INFINITY) ? 0.f : -m_run;
         // pass 2: p = 2^(s * scale - m), packed as bf16 pairs into the already-read
-        // first half of the S buffer (P columns 32h.. come from S columns 64h..).
-        // The scaling and the row sum run on packed fp32 pairs.
+        // first half of the S buffer (P columns 32h.. come from S columns 64h..), again
+        // one round trip.  The scaling and the row sum run on packed fp32 pairs.
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nbx2 = f2_pack(nb, nb);
         uint64_t lsx2 = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t s[64];
-          tmem_ld32(tl + s_col + 64 * h, s);
-          tmem_ld32(tl + s_col + 64 * h + 32, s + 32);
+        {
+          uint32_t s[128];
+          tmem_ld32(tl + s_col, s);
+          tmem_ld32(tl + s_col + 32, s + 32);
+          tmem_ld32(tl + s_col + 64, s + 64);
+          tmem_ld32(tl + s_col + 96, s + 96);
           tmem_wait_ld32(s);
           tie32(s + 32);
-          uint32_t pk[32];
+          tie32(s + 64);
+          tie32(s + 96);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), sl2x2, nbx2),
-                      x0, x1);
-            const float p0 = ex2(x0), p1 = ex2(x1);
-            lsx2 = f2_add(lsx2, f2_pack(p0, p1));
-            pk[c] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+          for (int h = 0; h < 2; ++h) {
+            // the packed pairs of keys 64 h .. 64 h + 63 overwrite s[32 h ..], already read
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(s[64 * h + 2 * c]), __uint_as_float(s[64 * h + 2 * c + 1])),
+                               sl2x2, nbx2),
+                        x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              lsx2 = f2_add(lsx2, f2_pack(p0, p1));
+              s[32 * h + c] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+            }
           }
-          tmem_st32(tl + s_col + 32 * h, pk);
+          tmem_st32(tl + s_col, s);
+          tmem_st32(tl + s_col + 32, s + 32);
         }
         float ls0, ls1;
         f2_unpack(lsx2, ls0, ls1);
