@@ -554,13 +554,17 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         tc_fence_after();
         const float inv = 1.f / l_run;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t o[32];
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          // 64 columns of the row's O per TMEM round trip (one wait covers all loads in
+          // flight), then their stores
+          uint32_t o[64];
           tmem_ld32(tl + o_col + c0, o);
+          tmem_ld32(tl + o_col + c0 + 32, o + 32);
           tmem_wait_ld32(o);
+          tie32(o + 32);
           if (row_ok) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
+            for (int e = 0; e < 64; e += 4)
               *reinterpret_cast<float4*>(oblk + (c0 + e) * 32) =
                   make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
                               __uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
