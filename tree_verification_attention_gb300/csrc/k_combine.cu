@@ -159,16 +159,29 @@ __global__ void __launch_bounds__(32 * WPB) combine_kernel(CombineArgs a) {
   const int cs = (int)(wid % per_group) % NCG;  // column-group set
   const GroupLoc R = locate_group(pr, qg);      // uniform over the warp
   if (!R.found) return;
-  const long long c = chunk_units(pr, R.T);
-  const int u0 = (int)(R.start / c);
-  const int np = (int)((R.start + R.tiles - 1) / c) - u0 + 1;
-  if ((long long)u0 + np - 1 + qg >= a.slots) {  // cannot happen for a consistent layout
+  // the workers that cover the group, and the slot of the first one's partial (the
+  // group's partials are in consecutive slots; see partial_slot)
+  long long slot0;
+  int np;
+  if (pr.share == 0) {
+    const long long c = chunk_units(pr, R.T);
+    const int u0 = (int)(R.start / c);
+    np = (int)((R.start + R.tiles - 1) / c) - u0 + 1;
+    slot0 = (long long)u0 + qg;
+  } else {
+    const long long cc = share_columns_per_team(pr, R.tiles);
+    const long long c0 = (long long)R.g * R.tiles;
+    const int k0 = (int)(c0 / cc);
+    np = (int)((c0 + R.tiles - 1) / cc) - k0 + 1;
+    slot0 = (long long)R.mp * (share_teams(pr) + pr.Hkv) + k0 + R.g;
+  }
+  if (slot0 + np - 1 >= a.slots) {  // cannot happen for a consistent layout
     if (lane == 0) set_status(a.status, kStatusInvalidArg);
     return;
   }
   ptx::pdl_wait();  // the partials (and every earlier write) are visible after this
   ptx::pdl_launch_dependents();
-  merge_rows<T, D, CG, NB>(pr, a.o_part, a.lse_part, R, (size_t)u0 + qg, np, rb, cs, lane, a.out, a.lse,
+  merge_rows<T, D, CG, NB>(pr, a.o_part, a.lse_part, R, (size_t)slot0, np, rb, cs, lane, a.out, a.lse,
                            a.status);
 }
 
@@ -224,10 +237,15 @@ cudaError_t launch_typed(const CombineArgs& a, cudaStream_t s) {
 
 // Partials per row group when every sequence is at its stated maximum size: the units
 // of one row group (prefix tiles + the tree tile) spread over ceil(tiles / chunk) + 1
-// workers at most.  Smaller sequences shrink the chunk and can raise the count; the
+// workers at most (stream-K), or over the teams that cover its KV head (shared mode).  Smaller sequences shrink the chunk and can raise the count; the
 // kernel loops over any number, this only sizes its first round of loads.
 int expected_partials(const Problem& pr) {
   const long long tiles = (pr.max_prefix + kKeyTile - 1) / kKeyTile + 1;
+  if (pr.share > 0) {  // a head's columns spread over ceil(tiles / columns per team) + 1 teams
+    const long long Q = pr.U / pr.share, C = (long long)pr.Hkv * tiles;
+    const long long cc = Q > 0 ? (C + Q - 1) / Q : 1;
+    return (int)((tiles + cc - 1) / cc + 1);
+  }
   const long long T = max_row_groups(pr) * tiles;
   const long long c = T > 0 ? (T + pr.U - 1) / pr.U : 1;
   return (int)((tiles + c - 1) / c + 1);

@@ -162,10 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long t_begin = 0, t_end = 0;
   auto schedule = [&]() {
     stage_problem(a.pr, pr_s, reinterpret_cast<int*>(smem + kBarOff + kCuOff), kCuCap);
-    const long long T_all = total_units(pr);
-    const long long chunk = chunk_units(pr, T_all);
-    t_begin = (long long)u * chunk;
-    t_end = min(T_all, t_begin + chunk);
+    worker_range(pr, u, t_begin, t_end, pr.share != 0);
   };
   if (params_only) schedule();
   cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
@@ -206,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long t = t_begin;
     Segment S;
     const uint64_t evict_first = policy_evict_first();  // K / V are read once
-    while (ok && next_segment(pr, t, t_end, S)) {
+    while (ok && next_segment(pr, u, t, t_end, S, pr.share != 0)) {
       const Loc& L = S.L;
       const int n = S.n, qb = sg & 1;
       if (sg >= 2 && !wait_or_abort(warp_wait(Q_EMPTY + 8 * qb, ((sg >> 1) - 1) & 1, abort_flag, wait_ns))) {
@@ -300,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Test hook: DRAIN's first phase completes only through this thread's own commit
       // below, so this wait runs out, exercising the timeout path (abort, drain, free).
       if (args.stall && !wait_or_abort(warp_wait(DRAIN, 0, abort_flag, wait_ns))) ok = false;
-      while (ok && next_segment(pr, t, t_end, S)) {
+      while (ok && next_segment(pr, u, t, t_end, S, pr.share != 0)) {
         const int n = S.n, qb = sg & 1;
         // ring order: K0, K1, then V_j followed by K_{j+2}; tile j belongs to stream j & 1
         auto rK = [&](int k) { return ring + (k < 2 ? k : 2 * k - 1); };
@@ -360,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bwait = [&](uint32_t bar, uint32_t parity) {
       return wait_or_abort(__all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, wait_ns)));
     };
-    while (ok && next_segment(pr, t, t_end, S)) {
+    while (ok && next_segment(pr, u, t, t_end, S, pr.share != 0)) {
       const Loc& L = S.L;
       const int n = S.n;
       const int node = (L.mp * 2 + (int)rank) * npt + r / G;  // local node id of this row
@@ -514,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lt = a0 * l_run + a1 * l1;
         const float inv = 1.f / lt;
         const float w0 = a0 * inv, w1 = a1 * inv;
-        const size_t slot = (size_t)u + L.q;
+        const size_t slot = (size_t)partial_slot(pr, u, L, pr.share != 0);
         if (slot >= (size_t)a.slots) {  // cannot happen for a consistent layout; never write past it
           set_status(a.status, kStatusInvalidArg);
           row_ok = false;

@@ -65,20 +65,18 @@ __global__ void __launch_bounds__(kThreads, 3) partials_simt_kernel(PartialArgs 
   const int kg = tid & 7;      // key group (QK) / column phase (PV)
   const int u = blockIdx.x;
   if (u == 0 && tid == 0) validate_sequences(pr, a.status);
-  const long long T_all = total_units(pr);
-  const long long c = chunk_units(pr, T_all);
-  long long t = (long long)u * c;
-  const long long t_end = min(T_all, t + c);
+  long long t = 0, t_end = 0;
+  worker_range(pr, u, t, t_end, pr.share != 0);
   const size_t kv_stride = (size_t)pr.Hkv * D;
 
-  while (t < t_end) {
-    const Loc L = locate_unit(pr, t);
-    const long long seg_end = min(t_end, L.start + L.tiles);
-    const int tile0 = L.tile;
-    const int tile1 = (int)(seg_end - L.start);
+  Segment S;
+  while (next_segment(pr, u, t, t_end, S, pr.share != 0)) {
+    const Loc L = S.L;
+    const int tile0 = S.tile0;
+    const int tile1 = S.tile0 + S.n;
     const bool has_tree = tile0 == 0;   // the tree tile is a row group's first unit
     const SeqInfo s = L.s;
-    const int slot = u + L.q;
+    const long long slot = partial_slot(pr, u, L, pr.share != 0);
     const bool slot_ok = slot < a.slots;  // cannot fail for a consistent layout
     if (!slot_ok && tid == 0) set_status(a.status, kStatusInvalidArg);
 
@@ -221,7 +219,6 @@ __global__ void __launch_bounds__(kThreads, 3) partials_simt_kernel(PartialArgs 
         }
       }
     }
-    t = seg_end;
   }
 }
 

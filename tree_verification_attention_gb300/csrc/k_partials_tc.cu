@@ -86,7 +86,7 @@ __device__ __forceinline__ int q_buffer(int W, int sg) { return W == 1 ? (sg & 1
 // Earlier segments that used the same buffer.
 __device__ __forceinline__ int q_use(int W, int sg) { return W == 1 ? (sg >> 1) : sg; }
 
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kShare>
 __global__ void __launch_bounds__(kThreadsTc, 1)
     partials_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -165,10 +165,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
   long long t_begin = 0, t_end = 0;
   auto schedule = [&]() {
     stage_problem(a.pr, pr_s, reinterpret_cast<int*>(smem + C::kBarOff + C::kCuOff), C::kCuCap);
-    const long long T_all = total_units(pr);
-    const long long chunk = chunk_units(pr, T_all);
-    t_begin = (long long)u * chunk;
-    t_end = min(T_all, t_begin + chunk);
+    worker_range(pr, u, t_begin, t_end, kShare);
   };
   if (params_only) schedule();
   pdl_wait();  // launched as a programmatic dependent: inputs are final after this
@@ -205,7 +202,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       Segment S;
       const uint32_t q_box_bytes = 64u * G * npt * 2u;
       const uint64_t evict_first = policy_evict_first();  // K/V are read once
-      while (ok && next_segment(pr, t, t_end, S)) {
+      while (ok && next_segment(pr, u, t, t_end, S, kShare)) {
         const Loc& L = S.L;
         const int qb = q_buffer(W, sg), quse = q_use(W, sg);
         if (quse > 0 && !warp_wait(Q_EMPTY + 8 * qb, (quse - 1) & 1, abort_flag, wait_ns)) { ok = false; break; }
@@ -319,7 +316,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       // Test hook: DRAIN's first phase completes only through this thread's own commit
       // below, so this wait runs out, exercising the timeout path (abort, drain, free).
       if (args.stall && !warp_wait(DRAIN, 0, abort_flag, wait_ns)) ok = false;
-      while (ok && next_segment(pr, t, t_end, S)) {
+      while (ok && next_segment(pr, u, t, t_end, S, kShare)) {
         const int n = S.n;
         qb = q_buffer(W, sg);
         if (!warp_wait(Q_FULL + 8 * qb, q_use(W, sg) & 1, abort_flag, wait_ns)) { ok = false; break; }
@@ -400,7 +397,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     bool ok = true;
     long long t = t_begin;
     Segment S;
-    while (ok && next_segment(pr, t, t_end, S)) {
+    while (ok && next_segment(pr, u, t, t_end, S, kShare)) {
       const Loc& L = S.L;
       const int n = S.n;
       const int mt = (W == 2) ? w : 0;
@@ -539,7 +536,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------------------- epilogue
-      const size_t slot = (size_t)u + L.q;
+      const size_t slot = (size_t)partial_slot(pr, u, L, kShare);
       if (slot >= (size_t)a.slots) {  // cannot happen for a consistent layout; never write past it
         set_status(a.status, kStatusInvalidArg);
         row_ok = false;
@@ -691,7 +688,7 @@ void tc_wait_settings(uint64_t* wait_ns, int* stall) {
 
 namespace {
 
-template <int D, bool kBF16>
+template <int D, bool kBF16, bool kShare>
 cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s) {
   constexpr CUtensorMapDataType type = kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const Problem& pr = a.pr;
@@ -705,17 +702,17 @@ cudaError_t launch_tc_typed(const PartialArgs& a, int W, int npt, cudaStream_t s
       !make_map(&mtv, type, a.tree_v, D, pr.Hkv, pr.node_capacity, 1, kKeyTile))
     return cudaErrorInvalidValue;
   constexpr int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = check_cuda(cudaFuncSetAttribute(partials_tc_kernel<D, kBF16>,
+  cudaError_t e = check_cuda(cudaFuncSetAttribute(partials_tc_kernel<D, kBF16, kShare>,
                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                              "cudaFuncSetAttribute(partials_tc_kernel)");
   if (e != cudaSuccess) return e;
   TcArgs ta{a, W, npt, 0, 0};
   tc_wait_settings(&ta.wait_ns, &ta.stall);
-  e = launch_pdl(partials_tc_kernel<D, kBF16>, dim3(pr.U), dim3(kThreadsTc), (size_t)smem, s, mq, mk, mv, mtk,
+  e = launch_pdl(partials_tc_kernel<D, kBF16, kShare>, dim3(pr.U), dim3(kThreadsTc), (size_t)smem, s, mq, mk, mv, mtk,
                  mtv, ta);
   if (e != cudaSuccess) {
     cudaFuncAttributes fa{};
-    cudaFuncGetAttributes(&fa, partials_tc_kernel<D, kBF16>);
+    cudaFuncGetAttributes(&fa, partials_tc_kernel<D, kBF16, kShare>);
     char what[160];
     snprintf(what, sizeof(what), "%s; kernel regs %d, max threads %d, smem %d+%d", cudaGetErrorString(e),
              fa.numRegs, fa.maxThreadsPerBlock, (int)fa.sharedSizeBytes, smem);
@@ -731,9 +728,15 @@ void set_tc_wait_limit(unsigned long long ns, int stall) {
   g_force_stall.store(stall != 0 ? 1 : 0, std::memory_order_relaxed);
 }
 
+template <bool kShare>
+cudaError_t launch_tc_mode(const PartialArgs& a, bool bf16, int W, int npt, cudaStream_t s) {
+  if (bf16)
+    return a.pr.d == 64 ? launch_tc_typed<64, true, kShare>(a, W, npt, s) : launch_tc_typed<128, true, kShare>(a, W, npt, s);
+  return a.pr.d == 64 ? launch_tc_typed<64, false, kShare>(a, W, npt, s) : launch_tc_typed<128, false, kShare>(a, W, npt, s);
+}
+
 cudaError_t launch_partials_tc(const PartialArgs& a, bool bf16, int W, int npt, cudaStream_t s) {
-  if (bf16) return a.pr.d == 64 ? launch_tc_typed<64, true>(a, W, npt, s) : launch_tc_typed<128, true>(a, W, npt, s);
-  return a.pr.d == 64 ? launch_tc_typed<64, false>(a, W, npt, s) : launch_tc_typed<128, false>(a, W, npt, s);
+  return a.pr.share != 0 ? launch_tc_mode<true>(a, bf16, W, npt, s) : launch_tc_mode<false>(a, bf16, W, npt, s);
 }
 
 }  // namespace tva

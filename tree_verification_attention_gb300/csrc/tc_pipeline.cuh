@@ -12,22 +12,6 @@ namespace tva {
 constexpr uint64_t kDrainNs = 2000000000ull;  // drain waits, and the default main-loop limit
 constexpr uint32_t kNegInfBits = 0xff800000u;
 
-// A maximal piece of a worker's unit range inside one row group: n key tiles from tile0.
-struct Segment {
-  Loc L;
-  int tile0, n;
-};
-
-__device__ __forceinline__ bool next_segment(const Problem& pr, long long& t, long long t_end, Segment& s) {
-  if (t >= t_end) return false;
-  s.L = locate_unit(pr, t);
-  const long long seg_end = min(t_end, s.L.start + s.L.tiles);
-  s.tile0 = s.L.tile;
-  s.n = (int)(seg_end - t);
-  t = seg_end;
-  return true;
-}
-
 // A bounded wait taken by a whole converged warp; the result is the same in every lane.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
   return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, abort, limit_ns));

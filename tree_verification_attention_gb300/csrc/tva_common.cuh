@@ -46,6 +46,12 @@ struct Problem {
   int RG;                    // rows per row group
   int U;                     // workers
   int max_prefix, max_nodes, kv_capacity, node_capacity;
+  // 0: workers take contiguous ranges of units (stream-K).  S >= 2 (one sequence whose
+  // KV heads have S row groups): workers form teams of S; team k takes a contiguous
+  // range of (KV head, key tile) columns and its member r computes row group r over it,
+  // so the team's S workers stream the same K/V tiles together and DRAM serves each
+  // tile once (the others read it from L2).
+  int share;
 };
 
 struct SeqInfo {
@@ -229,6 +235,80 @@ __device__ __forceinline__ bool locate_row(const Problem& pr, int n, int h, RowL
   }
   R.T = acc;
   return found;
+}
+
+// ---- A worker's work.  Walk positions are units in stream-K mode and (KV head, key
+// tile) columns of the one sequence in shared mode; a segment is a maximal run of a
+// worker's positions inside one row group.
+struct Segment {
+  Loc L;
+  int tile0, n;
+};
+
+// Shared mode: teams, and the columns a team takes.
+__device__ __forceinline__ int share_teams(const Problem& pr) { return pr.U / pr.share; }
+__device__ __forceinline__ long long share_columns_per_team(const Problem& pr, int tiles) {
+  const long long C = (long long)pr.Hkv * tiles;
+  const int Q = share_teams(pr);
+  return (C + Q - 1) / Q;
+}
+
+// Worker u's walk positions [t0, t1).  `shared` is pr.share != 0; kernels that know it
+// at compile time pass a constant, so the other mode's code is not in them.
+__device__ __forceinline__ void worker_range(const Problem& pr, int u, long long& t0, long long& t1, bool shared) {
+  if (!shared) {
+    const long long T = total_units(pr);
+    const long long c = chunk_units(pr, T);
+    t0 = (long long)u * c;
+    t1 = t0 + c < T ? t0 + c : T;
+    return;
+  }
+  const SeqInfo s = seq_info(pr, 0);
+  const int MP = seq_groups(pr, s.m), tiles = seq_tiles(s.P);
+  const int k = u / pr.share, r = u - k * pr.share;
+  t0 = t1 = 0;
+  if (k >= share_teams(pr) || r >= MP) return;  // no such row group, or a spare worker
+  const long long C = (long long)pr.Hkv * tiles, cc = share_columns_per_team(pr, tiles);
+  t0 = k * cc < C ? k * cc : C;
+  t1 = t0 + cc < C ? t0 + cc : C;
+}
+
+// The segment of worker u's walk that starts at t; advances t past it.
+__device__ __forceinline__ bool next_segment(const Problem& pr, int u, long long& t, long long t_end, Segment& seg,
+                                             bool shared) {
+  if (t >= t_end) return false;
+  long long end;
+  if (!shared) {
+    seg.L = locate_unit(pr, t);
+    end = seg.L.start + seg.L.tiles;
+  } else {
+    Loc& L = seg.L;
+    L.s = seq_info(pr, 0);
+    L.b = 0;
+    L.MP = seq_groups(pr, L.s.m);
+    L.tiles = seq_tiles(L.s.P);
+    L.g = (int)(t / L.tiles);
+    L.mp = u % pr.share;
+    L.tile = (int)(t - (long long)L.g * L.tiles);
+    L.q = L.g * L.MP + L.mp;
+    L.start = (long long)L.q * L.tiles;
+    end = (long long)(L.g + 1) * L.tiles;
+  }
+  if (end > t_end) end = t_end;
+  seg.tile0 = seg.L.tile;
+  seg.n = (int)(end - t);
+  t = end;
+  return true;
+}
+
+// The workspace slot of worker u's partial for the row group of L.  Stream-K: u + q
+// (a worker's row groups are consecutive, so no two (worker, group) pairs collide).
+// Shared mode, team k, member r, KV head g: r (Q + Hkv) + k + g (the teams covering a head
+// are consecutive, so k + g is unique for each r, and a group's partials are adjacent).
+__device__ __forceinline__ long long partial_slot(const Problem& pr, int u, const Loc& L, bool shared) {
+  if (!shared) return (long long)u + L.q;
+  const int k = u / pr.share, r = u - k * pr.share;
+  return (long long)r * (share_teams(pr) + pr.Hkv) + k + L.g;
 }
 
 // Partial-output layout.  A row group of RG = W * MT rows (W M-tiles of MT =

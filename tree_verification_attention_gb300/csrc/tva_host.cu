@@ -110,7 +110,11 @@ tva_status make_layout(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
   pr.U = dtype == TVA_FP32 ? sms * tva::simt_workers_per_sm() : (L->pair ? sms / 2 : sms);
   pr.max_prefix = max_prefix; pr.max_nodes = max_nodes;
   pr.kv_capacity = kv_cap; pr.node_capacity = node_cap;
-  const long long groups = (long long)B * Hkv * ((max_nodes + W * npt - 1) / (W * npt));
+  const int mp_max = (max_nodes + W * npt - 1) / (W * npt);  // row groups per KV head
+  const long long groups = (long long)B * Hkv * mp_max;
+  // One sequence whose KV heads have several row groups: teams of workers, one member per
+  // row group, stream the same K/V tiles together, so each is read from DRAM once.
+  pr.share = (B == 1 && mp_max >= 2 && pr.U >= mp_max) ? mp_max : 0;
   L->slots = pr.U + groups;
   const size_t rgp = (size_t)W * 128;  // padded rows per slot (see o_part_offset)
   L->o_bytes = align256((size_t)L->slots * rgp * d * sizeof(float));
