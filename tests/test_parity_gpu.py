@@ -74,6 +74,38 @@ def test_edge_cases_match_oracle(spec):
     _gpu.assert_close(w, out, lse, o_ref, l_ref, str(spec))
 
 
+# One sequence with several row groups per KV head runs the shared-K/V schedule (teams of
+# workers, one member per row group, over (KV head, key tile) columns): an empty prefix
+# (8 columns for 38 teams), head_dim 64 in fp16, the fp32 kernel, and a stated max_nodes
+# above the tree's size (team members whose row group does not exist).
+SHARED = [
+    dict(batch=1, Hq=64, Hkv=8, d=128, prefix=0, m=128, tree="random", dtype="bf16", vocab=8),
+    dict(batch=1, Hq=32, Hkv=8, d=64, prefix=5000, m=100, tree="random", dtype="fp16", vocab=8),
+    dict(batch=1, Hq=16, Hkv=2, d=128, prefix=3000, m=128, tree="random", dtype="fp32", vocab=8),
+    dict(batch=1, Hq=32, Hkv=8, d=128, prefix=2600, m=128, tree="depth_limited", max_depth=6, dtype="bf16", vocab=8),
+]
+
+
+@pytest.mark.parametrize("spec", SHARED, ids=[f"shared{i}" for i in range(len(SHARED))])
+def test_shared_kv_schedule_matches_oracle(spec):
+    w = workloads.make_workload(1, seed=91, **spec)
+    out, lse, st = _gpu.run_attention(w)
+    assert st == 0
+    o_ref, l_ref = _gpu.oracle_attention(w)
+    _gpu.assert_close(w, out, lse, o_ref, l_ref, str(spec))
+
+
+def test_shared_kv_schedule_with_a_loose_node_bound():
+    """max_nodes = 128 at G = 4 asks for two row groups per head; the 40-node tree has one,
+    so every team's second member has nothing to do."""
+    w = workloads.make_workload(1, seed=92, batch=1, Hq=32, Hkv=8, d=128, prefix=1700, m=40, tree="random",
+                                dtype="bf16", vocab=8)
+    out, lse, st = _gpu.run_attention(w, max_nodes=128)
+    assert st == 0
+    o_ref, l_ref = _gpu.oracle_attention(w)
+    _gpu.assert_close(w, out, lse, o_ref, l_ref, "loose node bound")
+
+
 def test_loose_bounds_and_capacity_do_not_change_results():
     """max_prefix_len / max_nodes larger than needed, k_cache with spare rows."""
     w = workloads.make_workload(4, prefix=(50, 400), batch=3, m=20)
