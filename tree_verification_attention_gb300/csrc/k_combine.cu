@@ -163,7 +163,11 @@ __global__ void __launch_bounds__(32 * WPB) combine_kernel(CombineArgs a) {
   // group's partials are in consecutive slots; see partial_slot)
   long long slot0;
   int np;
-  if (pr.share == 0) {
+  if (pr.share == 0 && pr.align > 0) {  // the group's own workers, the first min(align, tiles) busy
+    const int u0 = (int)qg * pr.align;
+    np = R.tiles < pr.align ? R.tiles : pr.align;
+    slot0 = (long long)u0 + qg;
+  } else if (pr.share == 0) {
     const long long c = chunk_units(pr, R.T);
     const int u0 = (int)(R.start / c);
     np = (int)((R.start + R.tiles - 1) / c) - u0 + 1;
@@ -241,6 +245,7 @@ cudaError_t launch_typed(const CombineArgs& a, cudaStream_t s) {
 // kernel loops over any number, this only sizes its first round of loads.
 int expected_partials(const Problem& pr) {
   const long long tiles = (pr.max_prefix + kKeyTile - 1) / kKeyTile + 1;
+  if (pr.share == 0 && pr.align > 0) return (int)std::min<long long>(pr.align, tiles);
   if (pr.share > 0) {  // a head's columns spread over ceil(tiles / columns per team) + 1 teams
     const long long Q = pr.U / pr.share, C = (long long)pr.Hkv * tiles;
     const long long cc = Q > 0 ? (C + Q - 1) / Q : 1;

@@ -52,6 +52,11 @@ struct Problem {
   // so the team's S workers stream the same K/V tiles together and DRAM serves each
   // tile once (the others read it from L2).
   int share;
+  // 0, or (one sequence, one row group per KV head, Hkv dividing U) the workers per row
+  // group: each row group's tiles are split evenly over its own workers, so no worker's
+  // range crosses into another row group (stream-K ranges do, and such a worker pays a
+  // second segment - epilogue, Q copy, tree tile - in the middle of its stream).
+  int align;
 };
 
 struct SeqInfo {
@@ -257,6 +262,17 @@ __device__ __forceinline__ long long share_columns_per_team(const Problem& pr, i
 // at compile time pass a constant, so the other mode's code is not in them.
 __device__ __forceinline__ void worker_range(const Problem& pr, int u, long long& t0, long long& t1, bool shared) {
   if (!shared) {
+    if (pr.align > 0) {  // worker j of row group q: its share of the group's tiles
+      const SeqInfo s = seq_info(pr, 0);
+      const int tiles = seq_tiles(s.P), q = u / pr.align, j = u - q * pr.align;
+      t0 = t1 = 0;
+      if (q >= pr.Hkv * seq_groups(pr, s.m)) return;
+      const int base = tiles / pr.align, extra = tiles - base * pr.align;
+      const long long start = (long long)q * tiles + (long long)j * base + (j < extra ? j : extra);
+      t0 = start;
+      t1 = start + base + (j < extra ? 1 : 0);
+      return;
+    }
     const long long T = total_units(pr);
     const long long c = chunk_units(pr, T);
     t0 = (long long)u * c;

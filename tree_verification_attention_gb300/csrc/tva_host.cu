@@ -115,6 +115,9 @@ tva_status make_layout(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
   // One sequence whose KV heads have several row groups: teams of workers, one member per
   // row group, stream the same K/V tiles together, so each is read from DRAM once.
   pr.share = (B == 1 && mp_max >= 2 && pr.U >= mp_max) ? mp_max : 0;
+  // One sequence with one row group per KV head: split each head's tiles over its own
+  // U / Hkv workers when Hkv divides U (see Problem::align).
+  pr.align = (B == 1 && mp_max == 1 && pr.U % Hkv == 0) ? pr.U / Hkv : 0;
   L->slots = pr.U + groups;
   const size_t rgp = (size_t)W * 128;  // padded rows per slot (see o_part_offset)
   L->o_bytes = align256((size_t)L->slots * rgp * d * sizeof(float));
