@@ -434,10 +434,12 @@ def main():
     att_ms, att_iso = timed(lambda: attn(d), 3)
     k1, k1_iso = timed(lambda: step(d), 7)
     # The CTA-pair partials kernel (a diagnostic selection of the library: cta_group::2,
-    # M = 256, each SM loading half of every K/V tile), timed the same way for comparison;
-    # it applies to two-M-tile row groups at head_dim 128 in 16-bit types.
-    pair_applies = (w.dtype != "fp32" and w.head_dim == 128
-                    and int(w.tree_sizes.max()) * (w.num_q_heads // w.num_kv_heads) > 128)
+    # M = 256, each SM loading half of every K/V tile), timed the same way for comparison
+    # where the library applies it (two-M-tile row groups at head_dim 128, 16-bit types).
+    workers_default = api.num_workers(params)
+    api.diag_use_cta_pair(True)
+    pair_applies = api.num_workers(params) != workers_default   # the pair runs one worker per two SMs
+    api.diag_use_cta_pair(False)
     pair_ms = pair_iso = None
     if pair_applies:
         api.diag_use_cta_pair(True)

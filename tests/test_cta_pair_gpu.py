@@ -2,7 +2,8 @@
 tva_diag_use_cta_pair diagnostic), against the float64 oracle.
 
 The pair kernel applies to bf16 / fp16 problems at head_dim 128 whose row groups hold two
-M-tiles (max_nodes * G > 128).  Each case first checks that the selection took effect: the
+M-tiles (max_nodes * G > 128; a single sequence whose tree one-M-tile groups cover with
+fewer M-tiles gets those instead, and no pair).  Each case first checks that the selection took effect: the
 pair kernel runs one worker per two SMs.
 """
 import numpy as np
@@ -33,8 +34,7 @@ def _workers(w, t):
 CASES = [
     (3, dict(prefix=1500)),                                   # 64-node best-first tree
     (5, dict(prefix=900)),                                    # G = 8, 128 nodes: 4 row groups
-    (6, dict(prefix=1200)),                                   # fp16 beam tree, 68 nodes
-    (6, dict(prefix=700, batch=3)),
+    (6, dict(prefix=700, batch=3)),                           # fp16 beam trees, 68 nodes
     (1, dict(batch=2, Hq=12, Hkv=4, d=128, prefix=(77, 200), m=50, tree="random", dtype="bf16",
              vocab=8, seed=77)),                              # 126-row M-tiles
     (1, dict(batch=1, Hq=32, Hkv=8, d=128, prefix=300, m=128, tree="random", dtype="fp16",

@@ -93,7 +93,16 @@ tva_status make_layout(int B, int Hq, int Hkv, int d, int dtype, int max_prefix,
   // Row groups hold whole nodes: an M-tile of 128 rows holds npt = floor(128 / G) nodes
   // (all G query heads of a node), and a row group W <= 2 M-tiles.
   const int npt = 128 / G;
-  const int W = (max_nodes > npt) ? 2 : 1;
+  int W = (max_nodes > npt) ? 2 : 1;
+  // One sequence whose tree needs several row groups: its row groups are computed by teams
+  // that share K/V (Problem::share), so the group size is free; one-M-tile groups win when
+  // they cover the tree with fewer M-tiles (a 68-node tree at 32 nodes per M-tile: 3
+  // against 2 x 2 - the second two-M-tile group would hold 4 nodes).
+  if (B == 1 && W == 2) {
+    const int mt1 = (max_nodes + npt - 1) / npt;
+    const int mt2 = 2 * ((max_nodes + 2 * npt - 1) / (2 * npt));
+    if (mt1 < mt2) W = 1;
+  }
   L->npt = npt;
   L->W = W;
   Problem& pr = L->pr;
