@@ -28,8 +28,9 @@ def _lib():
 
 
 @pytest.mark.parametrize("cfg,over", [(3, dict(prefix=1500, m=40)), (6, dict(prefix=700, batch=3)),
-                                      (1, dict(d=64, Hq=8, Hkv=2, prefix=600, m=20, dtype="bf16"))],
-                         ids=["bf16-d128-two-mtiles", "fp16-d128-batch", "bf16-d64"])
+                                      (1, dict(d=64, Hq=8, Hkv=2, prefix=600, m=20, dtype="bf16")),
+                                      (5, dict(prefix=900))],
+                         ids=["bf16-d128-two-mtiles", "fp16-d128-batch", "bf16-d64", "bf16-shared-kv-teams"])
 def test_expired_wait_reports_timeout_and_the_next_call_is_exact(cfg, over):
     w = workloads.make_workload(cfg, **over)
     t = _gpu.to_device(w)
