@@ -18,6 +18,12 @@
 // share a slot, because worker u+1 starting inside group q-1 would contradict worker
 // u reaching group q.  Partials therefore need at most U + Q slots (Q row groups).
 //
+// Two refinements for one sequence (see Problem::align and Problem::share): with one
+// row group per KV head, each head's tiles are split evenly over its own workers (no
+// range crosses a group); with several, workers form teams, one member per row group,
+// that walk the same (KV head, key tile) columns side by side, so the K/V tiles come
+// from DRAM once; a member's partials go to slots r (Q + Hkv) + k + g.
+//
 // Both the partials kernels and the combine kernel recompute this map from
 // cu_prefix / cu_nodes, so no schedule table is stored.
 #pragma once
