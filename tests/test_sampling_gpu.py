@@ -67,6 +67,23 @@ def test_bit_exact_against_oracle(B, V):
     assert (a_ref < np.diff(case[5])).any() and (a_ref > 0).any()   # both outcomes occur
 
 
+def test_masses_outside_the_fast_split_range_are_exact():
+    """Unnormalised nonnegative masses with entries planted at 2 and above: the slice sums
+    take the split fp32 form only for rounds whose masses all lie in [0, 2) and sum the
+    other rounds again on the integer path, so the draws stay bit-exact."""
+    rng = np.random.default_rng(57)
+    p, q, draft, ua, us, cu = _random_case(rng, 5, 128256)
+    p, q = (4 * p).astype(np.float32), (4 * q).astype(np.float32)
+    for rows in (p, q):
+        for r in range(rows.shape[0]):
+            at = rng.choice(rows.shape[1], 6, replace=False)
+            rows[r, at] = rng.uniform(2.0, 300.0, 6).astype(np.float32)
+    a_gpu, o_gpu = _gpu_verify(p, q, draft, ua, us, cu)
+    a_ref, o_ref = oracle.verify_chain_sampling(p, q, draft, ua, us, cu)
+    np.testing.assert_array_equal(a_gpu, a_ref)
+    np.testing.assert_array_equal(o_gpu, o_ref)
+
+
 def test_gpu_outputs_follow_the_target_distribution():
     _pins.check_sampling_marginals(_gpu_verify, np.random.default_rng(51), n=60000)
 

@@ -37,13 +37,42 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCluster = 8;
 constexpr int kUnroll = 8;
-constexpr float kQScale = 1099511627776.0f;  // 2^40
 constexpr float kUScale = 16777216.0f;       // 2^24
 
 __device__ __forceinline__ unsigned long long quant(float w) {
-  // w * 2^40 is exact (a power-of-two scale); truncation is the floor for w >= 0
-  return __float2ull_rz(fmaxf(w, 0.f) * kQScale);
+  // floor(max(w, 0) * 2^40) clamped to 64 bits (what a truncating float to u64 conversion
+  // of max(w, 0) * 2^40 gives), from the bits on the integer pipe: that conversion runs on
+  // the FP64 unit, and the slice sums do two per vocabulary entry.  With w = m * 2^(x - 150)
+  // (m the 24-bit significand, x the biased exponent), w * 2^40 = (m * 2^40) >> (150 - x),
+  // where m * 2^40 fills the 64 bits exactly.  Negatives, -0 and NaN give 0, w < 2^-40
+  // (denormals included) gives 0, and w >= 2^24 (+inf included) gives 2^64 - 1.
+  const uint32_t b = __float_as_uint(w);
+  const unsigned long long m40 = (unsigned long long)((b & 0x7fffffu) | 0x800000u) << 40;
+  const unsigned long long q = m40 >> min(63u, 150u - min(150u, b >> 23));
+  if (b > 0x7f800000u || b < 0x2b800000u) return 0ull;   // sign bit or NaN; below 2^-40
+  return b >= 0x4b800000u ? ~0ull : q;                   // at or above 2^24
 }
+
+// The slice sums' form of quant() for w in [0, 2): floor(w * 2^40) = H * 2^23 + L with
+// H = floor(w * 2^17) and L = floor(frac(w * 2^17) * 2^23), each < 2^23, found by FMAs
+// that round toward zero onto the integer grid of [2^23, 2^24) (w * 2^17 + 2^23 lies in
+// it, so its rounding is 2^23 + H; the fraction w * 2^17 - H is exact in fp32, and
+// frac * 2^23 + 2^23 rounds to 2^23 + L).  H and L go to 32-bit sums (one 32-entry round
+// stays below 2^28); a round that saw any w outside [0, 2) (sign bit or bit 30 set in
+// the OR of the entries' bits) is summed again with quant().
+struct SplitSum {
+  uint32_t h = 0, l = 0;
+  __device__ __forceinline__ void add(float w) {
+    const float t = __fmaf_rz(w, 0x1p17f, 0x1p23f);                 // 2^23 + H
+    const float lo = __fmaf_rz(__fmaf_rn(w, 0x1p17f, __fsub_rn(0x1p23f, t)), 0x1p23f, 0x1p23f);
+    h += __float_as_uint(t) - 0x4b000000u;
+    l += __float_as_uint(lo) - 0x4b000000u;
+  }
+  __device__ __forceinline__ unsigned long long value() const {
+    return ((unsigned long long)h << 23) + l;
+  }
+};
+constexpr uint32_t kSplitOutside = 0xc0000000u;   // sign bit or exponent >= 128: w outside [0, 2)
 
 __device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long x) {
 #pragma unroll
@@ -122,12 +151,35 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
     }
   };
   unsigned long long cr = 0, cp = 0;   // this lane's sums
+  SplitSum hr, hp;                     // this round's residual and p sums
+  uint32_t seen = 0;                   // OR of this round's entries' bits
   auto accumulate = [&](const float (&pv)[4], const float (&qv)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float r = fmaxf(0.f, __fsub_rn(pv[e], qv[e]));
+      hr.add(r);
+      hp.add(pv[e]);
+      seen |= __float_as_uint(r) | __float_as_uint(pv[e]);
+    }
+  };
+  auto accumulate_exact = [&](const float (&pv)[4], const float (&qv)[4]) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       cr += quant(fmaxf(0.f, __fsub_rn(pv[e], qv[e])));
       cp += quant(pv[e]);
     }
+  };
+  // end of a round: fold the 32-bit split sums in, or redo the round exactly
+  auto close_round = [&](auto&& redo) {
+    if (seen & kSplitOutside) {
+      redo();
+    } else {
+      cr += hr.value();
+      cp += hp.value();
+    }
+    hr = SplitSum();
+    hp = SplitSum();
+    seen = 0;
   };
   if (vec) {
     // 16-byte rows with V a multiple of 4: every group of 4 starting below w1 is whole,
@@ -147,6 +199,13 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
         const float qv[4] = {q4[j].x, q4[j].y, q4[j].z, q4[j].w};
         accumulate(pv, qv);
       }
+      close_round([&] {
+        for (int j = 0; j < kUnroll; ++j) {
+          const float pv[4] = {p4[j].x, p4[j].y, p4[j].z, p4[j].w};
+          const float qv[4] = {q4[j].x, q4[j].y, q4[j].z, q4[j].w};
+          accumulate_exact(pv, qv);
+        }
+      });
     }
   } else {
     for (int base = w0; base < w1; base += 128 * kUnroll) {
@@ -162,6 +221,9 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
       }
 #pragma unroll
       for (int j = 0; j < kUnroll; ++j) accumulate(pv[j], qv[j]);
+      close_round([&] {
+        for (int j = 0; j < kUnroll; ++j) accumulate_exact(pv[j], qv[j]);
+      });
     }
   }
   cr = warp_sum_u64(cr);
