@@ -15,14 +15,15 @@
 //
 // A sequence is served by a cluster of kCluster CTAs.  Every CTA repeats the cheap
 // acceptance tests (so all of them take the same decisions from the same inputs and
-// reach the cluster barriers together), then sums the quantised masses of its slice of
-// the vocabulary row with many loads in flight.  The slice is cut into one contiguous
+// reach the cluster barriers together), then sums the quantised masses of the draw (the
+// residual after a rejection, else p) over its slice of the vocabulary row with many
+// loads in flight; a residual whose quantised total is empty is summed again as p.  The slice is cut into one contiguous
 // chunk per warp, and a warp reads its chunk with coalesced 16-byte loads (lane l takes
 // every 32nd group of 4 entries), so each load instruction covers 512 contiguous bytes.
-// The slice sums are exchanged through distributed shared memory; in the CTA whose
-// slice holds the threshold the warp sums locate the warp chunk, whose lanes then take
-// contiguous pieces of it: a warp scan of their sums picks the piece, and one lane walks
-// it entry by entry.
+// Each CTA pushes its slice sum into the shared memory of every CTA of the cluster
+// (distributed shared memory) before a cluster barrier, after which no CTA reads a peer.  In the CTA whose slice holds the threshold the warp sums locate the warp chunk,
+// which the whole CTA then cuts into one contiguous piece per thread: a block scan of the
+// pieces' sums picks the piece, and its thread walks it entry by entry.
 #include <cooperative_groups.h>
 
 #include "tc_ptx.cuh"
@@ -37,7 +38,6 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCluster = 8;
 constexpr int kUnroll = 8;
-constexpr float kUScale = 16777216.0f;       // 2^24
 
 __device__ __forceinline__ unsigned long long quant(float w) {
   // floor(max(w, 0) * 2^40) clamped to 64 bits (what a truncating float to u64 conversion
@@ -90,8 +90,9 @@ __device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long l
 }
 
 struct __align__(16) ClusterShared {
-  unsigned long long red[2 * kWarps];   // per-warp sums: residual masses, then p
-  unsigned long long slice[2];   // this CTA's residual and p sums (read by the cluster)
+  unsigned long long red[kWarps];            // per-warp mass sums of the current pass
+  unsigned long long slice[2][kCluster];     // every CTA's slice sum per pass, pushed by its owner
+  unsigned long long scan[kWarps];           // the draw's per-warp piece totals
   int first, tok;
 };
 
@@ -150,110 +151,102 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
       for (int e = 0; e < 4; ++e) out[e] = v + e < end ? __ldg(row + v + e) : 0.f;
     }
   };
-  unsigned long long cr = 0, cp = 0;   // this lane's sums
-  SplitSum hr, hp;                     // this round's residual and p sums
-  uint32_t seen = 0;                   // OR of this round's entries' bits
-  auto accumulate = [&](const float (&pv)[4], const float (&qv)[4]) {
+  // The draw's masses are max(0, p - q) with q read as 0 when qm is null: the residual
+  // [p - q]_+ after a rejection, p for the bonus.  A residual whose quantised mass is empty
+  // is summed again as p in a second pass (every CTA of the cluster sees the same total,
+  // so all of them take it together).
+  const float* qm = qrow;
+  unsigned long long Z = 0, before = 0, mine = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    unsigned long long c = 0;   // this lane's sum
+    SplitSum hs;                // this round's split sums
+    uint32_t seen = 0;          // OR of this round's masses' bits
+    auto accumulate = [&](const float (&pv)[4], const float (&qv)[4]) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float r = fmaxf(0.f, __fsub_rn(pv[e], qv[e]));
-      hr.add(r);
-      hp.add(pv[e]);
-      seen |= __float_as_uint(r) | __float_as_uint(pv[e]);
-    }
-  };
-  auto accumulate_exact = [&](const float (&pv)[4], const float (&qv)[4]) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      cr += quant(fmaxf(0.f, __fsub_rn(pv[e], qv[e])));
-      cp += quant(pv[e]);
-    }
-  };
-  // end of a round: fold the 32-bit split sums in, or redo the round exactly
-  auto close_round = [&](auto&& redo) {
-    if (seen & kSplitOutside) {
-      redo();
-    } else {
-      cr += hr.value();
-      cp += hp.value();
-    }
-    hr = SplitSum();
-    hp = SplitSum();
-    seen = 0;
-  };
-  if (vec) {
-    // 16-byte rows with V a multiple of 4: every group of 4 starting below w1 is whole,
-    // so the loads are plain selects and all of them are issued before the first use
-    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int base = w0; base < w1; base += 128 * kUnroll) {
-      float4 p4[kUnroll], q4[kUnroll];
-#pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
-        const int v = base + 128 * j + 4 * lane;
-        p4[j] = v < w1 ? __ldg(reinterpret_cast<const float4*>(prow + v)) : zero;
-        q4[j] = (v < w1 && qrow != nullptr) ? __ldg(reinterpret_cast<const float4*>(qrow + v)) : zero;
+      for (int e = 0; e < 4; ++e) {
+        const float m = fmaxf(0.f, __fsub_rn(pv[e], qv[e]));
+        hs.add(m);
+        seen |= __float_as_uint(m);
       }
+    };
+    auto accumulate_exact = [&](const float (&pv)[4], const float (&qv)[4]) {
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
-        const float pv[4] = {p4[j].x, p4[j].y, p4[j].z, p4[j].w};
-        const float qv[4] = {q4[j].x, q4[j].y, q4[j].z, q4[j].w};
-        accumulate(pv, qv);
-      }
-      close_round([&] {
+      for (int e = 0; e < 4; ++e) c += quant(fmaxf(0.f, __fsub_rn(pv[e], qv[e])));
+    };
+    // end of a round: fold the 32-bit split sums in, or redo the round exactly
+    auto close_round = [&](auto&& redo) {
+      if (seen & kSplitOutside) redo();
+      else c += hs.value();
+      hs = SplitSum();
+      seen = 0;
+    };
+    if (vec) {
+      // 16-byte rows with V a multiple of 4: every group of 4 starting below w1 is whole,
+      // so the loads are plain selects and all of them are issued before the first use
+      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int base = w0; base < w1; base += 128 * kUnroll) {
+        float4 p4[kUnroll], q4[kUnroll];
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j) {
+          const int v = base + 128 * j + 4 * lane;
+          p4[j] = v < w1 ? __ldg(reinterpret_cast<const float4*>(prow + v)) : zero;
+          q4[j] = (v < w1 && qm != nullptr) ? __ldg(reinterpret_cast<const float4*>(qm + v)) : zero;
+        }
+#pragma unroll
         for (int j = 0; j < kUnroll; ++j) {
           const float pv[4] = {p4[j].x, p4[j].y, p4[j].z, p4[j].w};
           const float qv[4] = {q4[j].x, q4[j].y, q4[j].z, q4[j].w};
-          accumulate_exact(pv, qv);
+          accumulate(pv, qv);
         }
-      });
-    }
-  } else {
-    for (int base = w0; base < w1; base += 128 * kUnroll) {
-      float pv[kUnroll][4], qv[kUnroll][4];
-#pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
-        const int v = base + 128 * j + 4 * lane;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          pv[j][e] = v + e < w1 ? __ldg(prow + v + e) : 0.f;
-          qv[j][e] = (v + e < w1 && qrow != nullptr) ? __ldg(qrow + v + e) : 0.f;
-        }
+        close_round([&] {
+          for (int j = 0; j < kUnroll; ++j) {
+            const float pv[4] = {p4[j].x, p4[j].y, p4[j].z, p4[j].w};
+            const float qv[4] = {q4[j].x, q4[j].y, q4[j].z, q4[j].w};
+            accumulate_exact(pv, qv);
+          }
+        });
       }
+    } else {
+      for (int base = w0; base < w1; base += 128 * kUnroll) {
+        float pv[kUnroll][4], qv[kUnroll][4];
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) accumulate(pv[j], qv[j]);
-      close_round([&] {
-        for (int j = 0; j < kUnroll; ++j) accumulate_exact(pv[j], qv[j]);
-      });
+        for (int j = 0; j < kUnroll; ++j) {
+          const int v = base + 128 * j + 4 * lane;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            pv[j][e] = v + e < w1 ? __ldg(prow + v + e) : 0.f;
+            qv[j][e] = (v + e < w1 && qm != nullptr) ? __ldg(qm + v + e) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j) accumulate(pv[j], qv[j]);
+        close_round([&] {
+          for (int j = 0; j < kUnroll; ++j) accumulate_exact(pv[j], qv[j]);
+        });
+      }
     }
+    c = warp_sum_u64(c);
+    if (lane == 0) sh.red[warp] = c;
+    __syncthreads();
+    mine = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mine += sh.red[w];
+    // push this CTA's slice sum into every CTA of the cluster (itself included), so that
+    // after the barrier below nobody reads a peer's shared memory and any CTA may leave
+    if (threadIdx.x < kCluster) *cluster.map_shared_rank(&sh.slice[pass][rank], (int)threadIdx.x) = mine;
+    if (pass == 0 && threadIdx.x == 0) sh.tok = -1;
+    cluster.sync();   // every slice sum of this pass is in every CTA's shared memory
+    Z = 0;
+    before = 0;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) {
+      const unsigned long long x = sh.slice[pass][r];
+      if (r < rank) before += x;
+      Z += x;
+    }
+    if (Z > 0 || qm == nullptr) break;
+    qm = nullptr;   // the residual is empty: draw from p
   }
-  cr = warp_sum_u64(cr);
-  cp = warp_sum_u64(cp);
-  if (lane == 0) {
-    sh.red[warp] = cr;
-    sh.red[kWarps + warp] = cp;
-  }
-  __syncthreads();
-  unsigned long long sr = 0, sp = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    sr += sh.red[w];
-    sp += sh.red[kWarps + w];
-  }
-  if (threadIdx.x == 0) { sh.slice[0] = sr; sh.slice[1] = sp; }
-  cluster.sync();   // every slice sum is visible to the cluster
-
-  unsigned long long Zr = 0, Zp = 0, br = 0, bp = 0;
-  for (int r = 0; r < kCluster; ++r) {
-    const ClusterShared* peer = cluster.map_shared_rank(&sh, r);
-    const unsigned long long xr = peer->slice[0], xp = peer->slice[1];
-    if (r < rank) { br += xr; bp += xp; }
-    Zr += xr; Zp += xp;
-  }
-  cluster.sync();   // no CTA leaves (or reuses sh) while a peer may still read it
-
-  // residual when there is a rejection and its quantised mass is not empty, else p
-  const bool use_res = qrow != nullptr && Zr > 0;
-  const unsigned long long Z = use_res ? Zr : Zp, before = use_res ? br : bp;
-  const unsigned long long mine = use_res ? sr : sp;
   if (Z == 0) {   // p itself is empty (all masses below 2^-40 or invalid)
     if (rank == 0 && threadIdx.x == 0) {
       set_status(a.status, kStatusInvalidArg);
@@ -262,49 +255,66 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
     }
     return;
   }
-  const unsigned long long U = __float2ull_rz(us * kUScale);                 // < 2^24
+  // U = floor(u * 2^24) for u in [0, 1) from the bits (u = m * 2^(x - 150), so u * 2^24 =
+  // m / 2^(126 - x)); -0 reads as 0
+  const uint32_t ub = __float_as_uint(us) & 0x7fffffffu, ux = ub >> 23;
+  const unsigned long long U = ux < 103u ? 0ull : (unsigned long long)(((ub & 0x7fffffu) | 0x800000u) >> (126u - ux));
   const unsigned long long T = (__umul64hi(U, Z) << 40) | ((U * Z) >> 24);  // floor(U * Z / 2^24)
   if (!(before <= T && T < before + mine)) return;   // another CTA's slice holds the draw
 
-  // ---- the draw inside this slice: the warp chunk holding the threshold (from the warp
-  // sums), then inside it the lanes take contiguous pieces; a warp scan of the pieces'
-  // sums picks the one holding the threshold, and its lane walks it entry by entry
-  if (threadIdx.x == 0) sh.tok = -1;
-  __syncthreads();
-  const unsigned long long* wsum = use_res ? sh.red : sh.red + kWarps;
-  unsigned long long wexcl = before;
-  for (int w = 0; w < warp; ++w) wexcl += wsum[w];
-  if (wexcl <= T && T < wexcl + wsum[warp]) {   // uniform over the warp
-    const int LC = WC / 32;                      // entries per lane (a multiple of 4)
-    const int l0 = min(w1, w0 + lane * LC), l1 = min(w1, l0 + LC);
-    unsigned long long ls = 0;
-    for (int v = l0; v < l1; v += 4) {
-      float pv[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
-      load4(prow, v, l1, pv);
-      if (use_res) load4(qrow, v, l1, qv);
+  // ---- the draw inside this slice: the warp chunk holding the threshold (a scan of the
+  // warp sums across the lanes of each warp); the whole CTA then cuts that chunk into one
+  // piece of E entries per thread, a block scan of the pieces' sums picks the piece, and
+  // its thread walks it
+  const unsigned long long wl = lane < kWarps ? sh.red[lane] : 0ull;
+  const unsigned long long wincl = before + warp_incl_scan_u64(wl, lane);   // through chunk `lane`
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < kWarps && T < wincl);
+  const int cw = hit != 0u ? __ffs(hit) - 1 : kWarps - 1;   // the first chunk ending past T
+  const unsigned long long cexcl = __shfl_sync(0xffffffffu, wincl - wl, cw);
+  const int c0 = min(v1, v0 + cw * WC), c1 = min(v1, c0 + WC);
+  const int E = (WC + 4 * kThreads - 1) / (4 * kThreads) * 4;   // a multiple of 4
+  const int e0 = min(c1, c0 + (int)threadIdx.x * E), e1 = min(c1, e0 + E);
+  auto mass = [&](float pv, float qv) { return quant(fmaxf(0.f, __fsub_rn(pv, qv))); };
+  unsigned long long ls = 0, m0[4] = {0ull, 0ull, 0ull, 0ull};   // m0: the first group's masses
+  for (int v = e0; v < e1; v += 4) {
+    float pv[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
+    load4(prow, v, e1, pv);   // entries past e1 read as 0, whose mass is 0
+    if (qm != nullptr) load4(qm, v, e1, qv);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        ls += use_res ? quant(fmaxf(0.f, __fsub_rn(pv[e], qv[e]))) : quant(pv[e]);
+    for (int e = 0; e < 4; ++e) {
+      const unsigned long long x = mass(pv[e], qv[e]);
+      if (v == e0) m0[e] = x;
+      ls += x;
     }
-    const unsigned long long incl = warp_incl_scan_u64(ls, lane);
-    const unsigned long long lexcl = wexcl + incl - ls;   // running sum before this piece
-    if (lexcl <= T && T < lexcl + ls) {
-      unsigned long long run = lexcl;
-      int tok = -1;
-      for (int v = l0; v < l1 && tok < 0; v += 4) {
-        float pv[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
-        load4(prow, v, l1, pv);
-        if (use_res) load4(qrow, v, l1, qv);
+  }
+  const unsigned long long incl = warp_incl_scan_u64(ls, lane);
+  if (lane == 31) sh.scan[warp] = incl;
+  __syncthreads();
+  unsigned long long excl = cexcl + incl - ls;   // running sum before this thread's piece
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (tok < 0 && v + e < l1) {
-            run += use_res ? quant(fmaxf(0.f, __fsub_rn(pv[e], qv[e]))) : quant(pv[e]);
-            if (run > T) tok = v + e;
-          }
+  for (int w = 0; w < kWarps; ++w)
+    if (w < warp) excl += sh.scan[w];
+  if (excl <= T && T < excl + ls) {   // one thread: the pieces cut the chunk's mass
+    unsigned long long run = excl;
+    int tok = -1;
+    for (int v = e0; v < e1 && tok < 0; v += 4) {
+      unsigned long long x[4] = {m0[0], m0[1], m0[2], m0[3]};
+      if (v != e0) {   // a piece of more than one group reads the later groups again
+        float pv[4], qv[4] = {0.f, 0.f, 0.f, 0.f};
+        load4(prow, v, e1, pv);
+        if (qm != nullptr) load4(qm, v, e1, qv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = mass(pv[e], qv[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (tok < 0 && v + e < e1) {
+          run += x[e];
+          if (run > T) tok = v + e;
         }
       }
-      sh.tok = tok;
     }
+    sh.tok = tok;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
