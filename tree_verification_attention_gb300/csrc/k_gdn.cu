@@ -13,15 +13,20 @@
 // and the state itself is never updated here (the commit waits for the accepted branch).
 // The ratios gamma_i / gamma_j are products of alpha walked up from i to j (no division).
 //
-// One CTA (1024 threads) per (sequence, head).  q, k, v and the output are fp32 or bf16
-// (T); beta, alpha and the state are fp32, and all arithmetic is fp32 (bf16 inputs are
-// widened as they are staged; the output is rounded to T once):
-//   1. parents -> depth and path product (a thread per node), list offsets (a scan) and the
-//      depth-level order; K, Q and this CTA's columns of S_0 staged in shared memory;
-//   2. interaction values over ancestor pairs only: X (k.k) and Y (q.k), one pair per thread;
-//   3. K S_0 and Q S_0 for the thread's register tile (rows x 4 columns), with K and Q
-//      staged in shared memory and S_0 read as 16-byte vectors; the right-hand side goes
-//      to shared memory (over Q), gamma_i Q S_0 stays in registers;
+// D / 32 CTAs (1024 threads) per (sequence, head), each owning 32 columns of the output.
+// q, k, v and the output are fp32 or bf16 (T); beta, alpha and the state are fp32, and all
+// arithmetic is fp32 (bf16 inputs are widened as they are staged; the output is rounded to
+// T once):
+//   1. K, Q (16-byte loads, all issued before the first store) and this CTA's columns of
+//      S_0 staged in shared memory; parents -> depth and path product (a thread per node),
+//      list offsets (a scan) and the depth-level order;
+//   2. interaction values over ancestor pairs only: X (k.k) and Y (q.k), one pair per
+//      thread, which also records the pair's ancestor id (the lists that steps 4 and 5 walk);
+//   3. K S_0 and Q S_0: a warp takes 4 nodes (K and Q rows) x 16 columns, its lanes split
+//      the sum over the D rows of S_0 eight ways (k = 8 kk + lane % 8), so that each 16-byte
+//      load of S_0 brings distinct data to every lane, and a reduce-scatter of shuffles
+//      leaves each lane 4 finished sums; the right-hand side goes to shared memory over Q,
+//      gamma_i Q S_0 over K;
 //   4. forward substitution one depth level at a time (nodes of a level are independent);
 //   5. the output sum over each node's ancestors-or-self.
 #include <cuda_bf16.h>
@@ -34,8 +39,6 @@
 namespace tva {
 namespace {
 
-__device__ __forceinline__ float gdn_load(const float* p) { return __ldg(p); }
-__device__ __forceinline__ float gdn_load(const __nv_bfloat16* p) { return __bfloat162float(__ldg(p)); }
 // four consecutive elements (16-byte aligned for float, 8-byte for bf16)
 __device__ __forceinline__ float4 gdn_load4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
 __device__ __forceinline__ float4 gdn_load4(const __nv_bfloat16* p) {
@@ -58,15 +61,18 @@ template <int D>
 struct GdnSmem {
   static constexpr int kKPitch = D + 1;                 // padded rows: distinct rows, distinct banks
   static constexpr int kQPitch = D + 4;                 // padded, 16-byte aligned rows (Q, then W)
+  static constexpr int kSPitch = kCols + 4;             // 16-byte rows; the k-split reads hit 8 bank groups
   static constexpr int kWPitch = kCols + 4;
   static constexpr int kK = 0;                          // float [m][D+1]
   static constexpr int kQ = kK + ((kMaxNodes * kKPitch + 3) & ~3);   // float [m][D+4], later W [m][kCols+4]
-  static constexpr int kS = kQ + kMaxNodes * kQPitch;   // float [D][kCols]: this CTA's columns of S_0
-  static constexpr int kX = kS + D * kCols;             // float [kMaxPairs] (proper-ancestor pairs)
+  static constexpr int kS = kQ + kMaxNodes * kQPitch;   // float [D][kCols+4]: this CTA's columns of S_0
+  static constexpr int kX = kS + D * kSPitch;           // float [kMaxPairs] (proper-ancestor pairs)
   static constexpr int kY = kX + kMaxPairs;             // float [kMaxPairs] (ancestor-or-self pairs)
   static constexpr int kFloats = kY + kMaxPairs;
   static constexpr int kInts = 4 * kMaxNodes + 2 * (kMaxNodes + 2);   // par, dep, off, lvl, lvl0, fill
-  static constexpr size_t kBytes = (size_t)kFloats * 4 + (size_t)kInts * 4 + (size_t)kMaxNodes * 4 * 3;
+  // + gamma, alpha, beta (float [m]) and the pairs' ancestor ids (uint8 [kMaxPairs])
+  static constexpr size_t kBytes =
+      (size_t)kFloats * 4 + (size_t)kInts * 4 + (size_t)kMaxNodes * 4 * 3 + (size_t)kMaxPairs;
 };
 
 template <int D, typename T>
@@ -77,6 +83,7 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   float* sK = gsm + SM::kK;
   float* sQ = gsm + SM::kQ;
   float* sW = gsm + SM::kQ;                    // over Q once Q is no longer read
+  float* sG = gsm + SM::kK;                    // gamma_i Q S_0 [m][kCols+4], over K after step 3
   float* sS = gsm + SM::kS;
   float* sX = gsm + SM::kX;
   float* sY = gsm + SM::kY;
@@ -89,6 +96,7 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   float* s_gam = reinterpret_cast<float*>(s_fill + kMaxNodes + 2);   // gamma_i
   float* s_alpha = s_gam + kMaxNodes;
   float* s_beta = s_alpha + kMaxNodes;
+  uint8_t* s_anc = reinterpret_cast<uint8_t*>(s_beta + kMaxNodes);   // node id of each list entry
   __shared__ int s_maxdep, s_pairs;
 
   ptx::pdl_wait();
@@ -106,6 +114,8 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
   const int tid = threadIdx.x;
   const size_t hs = (size_t)a.H * D;   // stride between nodes in q / k / v / o
   const int c0 = cs * kCols;           // this CTA's first column of d_v
+  // v is read after the contractions: its rows start towards L2 now
+  if (tid < m) ptx::prefetch_l2(static_cast<const T*>(a.v) + (size_t)(n0 + tid) * hs + (size_t)h * D + c0);
 
   // ---- 1. K, Q, this CTA's columns of S_0 and the tree's scalars; then the bookkeeping
   for (int i = tid; i < m; i += kThreadsGdn) {
@@ -113,16 +123,43 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
     s_alpha[i] = __ldg(a.alpha + (size_t)(n0 + i) * a.H + h);
     s_beta[i] = __ldg(a.beta + (size_t)(n0 + i) * a.H + h);
   }
-  for (int e = tid; e < m * D; e += kThreadsGdn) {
-    const int i = e / D, r = e % D;
-    const size_t src = (size_t)(n0 + i) * hs + (size_t)h * D + r;
-    sK[i * SM::kKPitch + r] = gdn_load(static_cast<const T*>(a.k) + src);
-    sQ[i * SM::kQPitch + r] = gdn_load(static_cast<const T*>(a.q) + src);
-  }
-  const float* S0 = a.S0 + ((size_t)b * a.H + h) * D * D + c0;
-  for (int e = tid; e < D * (kCols / 4); e += kThreadsGdn) {
-    const int r = e / (kCols / 4), q4 = e % (kCols / 4);
-    *reinterpret_cast<float4*>(sS + r * kCols + 4 * q4) = __ldg(reinterpret_cast<const float4*>(S0 + (size_t)r * D) + q4);
+  {
+    constexpr int D4 = D / 4;
+    constexpr int kStage = (kMaxNodes * D4 + kThreadsGdn - 1) / kThreadsGdn;
+    constexpr int kS0 = (D * (kCols / 4) + kThreadsGdn - 1) / kThreadsGdn;
+    const float* S0 = a.S0 + ((size_t)b * a.H + h) * D * D + c0;
+    float4 kv[kStage], qv[kStage], sv[kS0];
+#pragma unroll
+    for (int t = 0; t < kStage; ++t) {   // every load issued before the first store
+      const int e = tid + t * kThreadsGdn;
+      if (e < m * D4) {
+        const size_t src = (size_t)(n0 + e / D4) * hs + (size_t)h * D + 4 * (e % D4);
+        kv[t] = gdn_load4(static_cast<const T*>(a.k) + src);
+        qv[t] = gdn_load4(static_cast<const T*>(a.q) + src);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kS0; ++t) {
+      const int e = tid + t * kThreadsGdn;
+      if (e < D * (kCols / 4))
+        sv[t] = __ldg(reinterpret_cast<const float4*>(S0 + (size_t)(e / (kCols / 4)) * D) + e % (kCols / 4));
+    }
+#pragma unroll
+    for (int t = 0; t < kStage; ++t) {
+      const int e = tid + t * kThreadsGdn;
+      if (e < m * D4) {
+        const int i = e / D4, r = 4 * (e % D4);
+        float* kd = sK + i * SM::kKPitch + r;
+        kd[0] = kv[t].x; kd[1] = kv[t].y; kd[2] = kv[t].z; kd[3] = kv[t].w;
+        *reinterpret_cast<float4*>(sQ + i * SM::kQPitch + r) = qv[t];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kS0; ++t) {
+      const int e = tid + t * kThreadsGdn;
+      if (e < D * (kCols / 4))
+        *reinterpret_cast<float4*>(sS + (e / (kCols / 4)) * SM::kSPitch + 4 * (e % (kCols / 4))) = sv[t];
+    }
   }
   if (tid == 0) s_maxdep = 0;
   for (int d = tid; d < kMaxNodes + 2; d += kThreadsGdn) s_lvl0[d] = 0;
@@ -210,42 +247,79 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
     }
     sX[pi] = aidx > 0 ? s_beta[i] * ratio * kk : 0.f;
     sY[pi] = ratio * qk;
+    s_anc[pi] = (uint8_t)j;
   }
 
-  // ---- 3. K S_0 and Q S_0 on this CTA's columns: thread -> 4 columns (cg) x rows rg, rg + RGS
-  constexpr int CG = kCols / 4;
-  constexpr int RGS = kThreadsGdn / CG;
-  constexpr int RPT = (kMaxNodes + RGS - 1) / RGS;
-  const int cg = tid % CG, rg = tid / CG;
-  float4 ks[RPT], qs[RPT];
+  // ---- 3. K S_0 and Q S_0 on this CTA's columns.  Warp w takes the column half w % 2
+  // (16 columns) and the nodes w / 2 + 16 t (t < 4) of each 64-node chunk; lane = kg + 8 cg
+  // takes columns 4 cg .. 4 cg + 3 of the half and the rows k = 8 kk + kg of S_0, so its 32
+  // partial sums (node slot t, K or Q, 4 columns: index 8 t + 4 kq + c) are reduced over
+  // the eight kg lanes by a reduce-scatter that leaves lane kg the sums 4 kg .. 4 kg + 3:
+  // node slot kg / 2, K (kg even) or Q (kg odd).
+  const int lane = tid & 31, warp = tid >> 5;
+  const int kg = lane & 7, cl = 16 * (warp & 1) + 4 * (lane >> 3), rset = warp >> 1;
+  const int kq = kg & 1;
+  float4 mine[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
 #pragma unroll
-  for (int t = 0; t < RPT; ++t) { ks[t] = make_float4(0.f, 0.f, 0.f, 0.f); qs[t] = ks[t]; }
-#pragma unroll 4
-  for (int r = 0; r < D; ++r) {
-    const float4 sv = *reinterpret_cast<const float4*>(sS + r * kCols + 4 * cg);
+  for (int chunk = 0; chunk < 2; ++chunk) {
+    const int base = 64 * chunk;
+    if (base >= m) break;   // uniform over the CTA
+    float acc[32];
 #pragma unroll
-    for (int t = 0; t < RPT; ++t) {
-      const int i = rg + t * RGS;
-      if (i < m) {
-        const float kv = sK[i * SM::kKPitch + r], qv = sQ[i * SM::kQPitch + r];
-        ks[t].x = fmaf(kv, sv.x, ks[t].x); ks[t].y = fmaf(kv, sv.y, ks[t].y);
-        ks[t].z = fmaf(kv, sv.z, ks[t].z); ks[t].w = fmaf(kv, sv.w, ks[t].w);
-        qs[t].x = fmaf(qv, sv.x, qs[t].x); qs[t].y = fmaf(qv, sv.y, qs[t].y);
-        qs[t].z = fmaf(qv, sv.z, qs[t].z); qs[t].w = fmaf(qv, sv.w, qs[t].w);
+    for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+#pragma unroll 2
+    for (int kk = 0; kk < D / 8; ++kk) {
+      const int k = 8 * kk + kg;
+      const float4 sv = *reinterpret_cast<const float4*>(sS + k * SM::kSPitch + cl);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = base + rset + 16 * t;
+        if (i < m) {   // uniform over the warp
+          const float kv = sK[i * SM::kKPitch + k], qv = sQ[i * SM::kQPitch + k];
+          float* ak = acc + 8 * t;
+          ak[0] = fmaf(kv, sv.x, ak[0]); ak[1] = fmaf(kv, sv.y, ak[1]);
+          ak[2] = fmaf(kv, sv.z, ak[2]); ak[3] = fmaf(kv, sv.w, ak[3]);
+          ak[4] = fmaf(qv, sv.x, ak[4]); ak[5] = fmaf(qv, sv.y, ak[5]);
+          ak[6] = fmaf(qv, sv.z, ak[6]); ak[7] = fmaf(qv, sv.w, ak[7]);
+        }
       }
     }
+    // reduce-scatter over kg (lane bits 2, 1, 0 of kg select index bits 4, 3, 2)
+#pragma unroll
+    for (int x = 0; x < 16; ++x) {
+      const bool up = (kg & 4) != 0;
+      const float give = up ? acc[x] : acc[16 + x], keep = up ? acc[16 + x] : acc[x];
+      acc[x] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+    }
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const bool up = (kg & 2) != 0;
+      const float give = up ? acc[x] : acc[8 + x], keep = up ? acc[8 + x] : acc[x];
+      acc[x] = keep + __shfl_xor_sync(0xffffffffu, give, 2);
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const bool up = (kg & 1) != 0;
+      const float give = up ? acc[x] : acc[4 + x], keep = up ? acc[4 + x] : acc[x];
+      acc[x] = keep + __shfl_xor_sync(0xffffffffu, give, 1);
+    }
+    mine[chunk] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   }
   __syncthreads();   // every read of Q is done: the buffer now takes the right-hand side
 #pragma unroll
-  for (int t = 0; t < RPT; ++t) {
-    const int i = rg + t * RGS;
+  for (int chunk = 0; chunk < 2; ++chunk) {
+    const int i = 64 * chunk + rset + 16 * (kg >> 1);
     if (i < m) {
-      const float4 vv = gdn_load4(static_cast<const T*>(a.v) + (size_t)(n0 + i) * hs + (size_t)h * D + c0 + 4 * cg);
-      const float bt = s_beta[i], gm = s_gam[i];
-      *reinterpret_cast<float4*>(sW + i * SM::kWPitch + 4 * cg) =
-          make_float4(bt * (vv.x - gm * ks[t].x), bt * (vv.y - gm * ks[t].y), bt * (vv.z - gm * ks[t].z),
-                      bt * (vv.w - gm * ks[t].w));
-      qs[t] = make_float4(gm * qs[t].x, gm * qs[t].y, gm * qs[t].z, gm * qs[t].w);
+      const float gm = s_gam[i];
+      const float4 x = mine[chunk];
+      if (kq == 0) {   // K S_0: the right-hand side beta_i (v_i - gamma_i S_0^T k_i)
+        const float4 vv = gdn_load4(static_cast<const T*>(a.v) + (size_t)(n0 + i) * hs + (size_t)h * D + c0 + cl);
+        const float bt = s_beta[i];
+        *reinterpret_cast<float4*>(sW + i * SM::kWPitch + cl) =
+            make_float4(bt * (vv.x - gm * x.x), bt * (vv.y - gm * x.y), bt * (vv.z - gm * x.z), bt * (vv.w - gm * x.w));
+      } else {         // Q S_0: gamma_i S_0^T q_i, parked over K (read by nobody after step 3)
+        *reinterpret_cast<float4*>(sG + i * SM::kWPitch + cl) = make_float4(gm * x.x, gm * x.y, gm * x.z, gm * x.w);
+      }
     }
   }
   __syncthreads();
@@ -256,33 +330,27 @@ __global__ void __launch_bounds__(kThreadsGdn, 1) gdn_tree_kernel(GdnArgs a) {
     const int l0 = s_lvl0[d], l1 = s_lvl0[d + 1];
     for (int e = tid; e < (l1 - l0) * kCols; e += kThreadsGdn) {
       const int i = s_lvl[l0 + e / kCols], cc = e % kCols;
+      const int off = s_off[i], dep = s_dep[i];
       float acc = sW[i * SM::kWPitch + cc];
-      int j = s_par[i];
-      for (int t = 1; t < s_dep[i]; ++t) {      // proper ancestors, nearest first
-        acc = fmaf(-sX[s_off[i] + t], sW[j * SM::kWPitch + cc], acc);
-        j = s_par[j];
-      }
+      for (int t = 1; t < dep; ++t)      // proper ancestors, nearest first
+        acc = fmaf(-sX[off + t], sW[s_anc[off + t] * SM::kWPitch + cc], acc);
       sW[i * SM::kWPitch + cc] = acc;
     }
     __syncthreads();
   }
 
-  // ---- 5. outputs
-#pragma unroll
-  for (int t = 0; t < RPT; ++t) {
-    const int i = rg + t * RGS;
-    if (i < m) {
-      float4 acc = qs[t];
-      int j = i;
-      for (int aa = 0; aa < s_dep[i]; ++aa) {   // ancestors-or-self, self first
-        const float y = sY[s_off[i] + aa];
-        const float4 w = *reinterpret_cast<const float4*>(sW + j * SM::kWPitch + 4 * cg);
-        acc.x = fmaf(y, w.x, acc.x); acc.y = fmaf(y, w.y, acc.y);
-        acc.z = fmaf(y, w.z, acc.z); acc.w = fmaf(y, w.w, acc.w);
-        j = s_par[j];
-      }
-      gdn_store4(static_cast<T*>(a.o) + (size_t)(n0 + i) * hs + (size_t)h * D + c0 + 4 * cg, acc);
+  // ---- 5. outputs: thread -> node tid / 8, columns 4 (tid % 8) .. + 3
+  for (int e = tid; e < m * (kCols / 4); e += kThreadsGdn) {
+    const int i = e / (kCols / 4), c = 4 * (e % (kCols / 4));
+    float4 acc = *reinterpret_cast<const float4*>(sG + i * SM::kWPitch + c);
+    const int off = s_off[i], dep = s_dep[i];
+    for (int aa = 0; aa < dep; ++aa) {   // ancestors-or-self, self first
+      const float y = sY[off + aa];
+      const float4 w = *reinterpret_cast<const float4*>(sW + s_anc[off + aa] * SM::kWPitch + c);
+      acc.x = fmaf(y, w.x, acc.x); acc.y = fmaf(y, w.y, acc.y);
+      acc.z = fmaf(y, w.z, acc.z); acc.w = fmaf(y, w.w, acc.w);
     }
+    gdn_store4(static_cast<T*>(a.o) + (size_t)(n0 + i) * hs + (size_t)h * D + c0 + c, acc);
   }
 }
 
