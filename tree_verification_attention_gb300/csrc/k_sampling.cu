@@ -41,8 +41,9 @@ constexpr int kUnroll = 8;
 
 __device__ __forceinline__ unsigned long long quant(float w) {
   // floor(max(w, 0) * 2^40) clamped to 64 bits (what a truncating float to u64 conversion
-  // of max(w, 0) * 2^40 gives), from the bits on the integer pipe: that conversion runs on
-  // the FP64 unit, and the slice sums do two per vocabulary entry.  With w = m * 2^(x - 150)
+  // of max(w, 0) * 2^40 gives), from the bits on the integer pipe (that conversion runs on
+  // the FP64 unit, which is slow here).  This exact form serves the draw and the rounds
+  // that SplitSum below cannot take.  With w = m * 2^(x - 150)
   // (m the 24-bit significand, x the biased exponent), w * 2^40 = (m * 2^40) >> (150 - x),
   // where m * 2^40 fills the 64 bits exactly.  Negatives, -0 and NaN give 0, w < 2^-40
   // (denormals included) gives 0, and w >= 2^24 (+inf included) gives 2^64 - 1.
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kThreads) sampling_kernel(SamplingArgs a) {
   const float* qrow = k < gamma ? a.q + (size_t)(g0 + k) * a.V : nullptr;
 
   // ---- this CTA's slice, cut into one contiguous chunk per warp (a multiple of 128
-  // entries): per-warp sums of the residual masses and of p
+  // entries): per-warp sums of the draw's masses
   const int S = ((a.V + kCluster - 1) / kCluster + 3) & ~3;
   const int v0 = min(a.V, rank * S), v1 = min(a.V, v0 + S);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
