@@ -67,6 +67,20 @@ def test_bit_exact_against_oracle(B, V):
     assert (a_ref < np.diff(case[5])).any() and (a_ref > 0).any()   # both outcomes occur
 
 
+@pytest.mark.parametrize("V", [600000, 600001])
+def test_large_vocabulary_multi_group_pieces(V):
+    """A vocabulary above about 262 K tokens gives each thread of the drawing CTA a piece
+    of more than one group of 4 entries (its walk reads the later groups again); V not a
+    multiple of 4 takes the scalar loads."""
+    rng = np.random.default_rng(V % 7)
+    case = _random_case(rng, 3, V, max_gamma=4, temp=4.0)
+    a_gpu, o_gpu = _gpu_verify(*case)
+    a_ref, o_ref = oracle.verify_chain_sampling(*case)
+    np.testing.assert_array_equal(a_gpu, a_ref)
+    np.testing.assert_array_equal(o_gpu, o_ref)
+    assert (a_ref < np.diff(case[5])).any() and (a_ref == np.diff(case[5])).any()   # residual and bonus draws
+
+
 def test_masses_outside_the_fast_split_range_are_exact():
     """Unnormalised nonnegative masses with entries planted at 2 and above: the slice sums
     take the split fp32 form only for rounds whose masses all lie in [0, 2) and sum the
