@@ -265,7 +265,8 @@ tva_status commit_accepted_kv(int batch, int num_kv_heads, int head_dim, tva_dty
  * Decisions: accept when p(x) >= q(x) or when u * q(x), rounded to fp32, is < p(x).
  * A draw is an inverse-CDF draw over masses quantised to 2^-40 and summed exactly as
  * integers (threshold floor(floor(u * 2^24) * Z / 2^24)), so it does not depend on the
- * order of the sums; an empty residual falls back to p.  A sequence with bad bounds, a
+ * order of the sums; an empty residual falls back to p.  p and q hold probabilities
+ * (finite, >= 0); a negative or NaN entry is read as mass 0.  A sequence with bad bounds, a
  * token outside [0, V), q(x) = 0 or a uniform outside [0, 1) gets accept_len 0,
  * out_token -1 and TVA_ERR_INVALID_ARG in *dev_status. */
 tva_status verify_chain_sampling(int batch, int vocab, int max_draft, long long p_rows, long long q_rows,
